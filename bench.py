@@ -1,0 +1,556 @@
+#!/usr/bin/env python
+"""Benchmark of the decode-attention hot path (append + split-KV decode + combine).
+
+Workload: the MHA decode sweep — B=1, 16 query heads on 16 KV heads, head_dim
+128, fp16, kv_len in {1024, 4096, 8192} with capacity = kv_len. One step is
+one decode token through every layer of a model whose layers each own a
+static cache: for each kv_len, `layers` caches (enough that the caches of one
+kv_len total at least 3x the L2 size, so every layer reads cold HBM), and for
+every layer an in-place append at kv_len - 1 followed by attention over the
+kv_len rows. The step is captured once in a CUDA graph from the public API
+calls and replayed; timing uses CUDA events on the launching stream.
+
+Printed: one JSON line with the whole-job achieved HBM GB/s over algorithmic
+bytes (K/V prefix read once + q read + out write + the appended rows), the
+us per layer-step for each kv_len, the decode kernel's roofline (its own
+launches timed with CUDA events placed around it), the end-to-end number
+with per-step host<->device copies, the fp64 CPU oracle timed on the host's
+cores, and the SM clocks seen during the run.
+
+--impl reference times the CPU oracle alone on a bounded sample of the same
+workload (the slow baseline arm).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import pathlib
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = pathlib.Path(__file__).resolve().parent
+if str(ROOT) not in sys.path:
+    sys.path.insert(0, str(ROOT))
+
+METRIC = "decode-attn achieved HBM GB/s (% of GB300 peak); µs per layer-step vs kv_len"
+UNIT = "GB/s"
+SWEEP = (1024, 4096, 8192)
+B, N_HEAD, N_KV_HEAD, HEAD_DIM = 1, 16, 16, 128
+ELEM = 2  # fp16
+WORKLOAD = ("MHA decode sweep: B=1, 16 query / 16 KV heads, head_dim 128, fp16, kv_len in {1024, 4096, 8192}, "
+            "capacity = kv_len, append at kv_len-1 then attend")
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0
+
+
+# ---------------------------------------------------------------------------
+# Byte model (algorithmic bytes: what the method must move at minimum).
+
+def attend_bytes(batch: int, n_head: int, n_kv_head: int, head_dim: int, kv_lens, elem: int = ELEM) -> int:
+    """K and V prefix rows read once, q read, out written."""
+    return 2 * elem * n_kv_head * head_dim * int(sum(kv_lens)) + 2 * elem * batch * n_head * head_dim
+
+
+def append_bytes(batch: int, n_kv_head: int, head_dim: int, elem: int = ELEM) -> int:
+    """k_new and v_new read, one K row and one V row written per (b, kv head)."""
+    return 4 * elem * batch * n_kv_head * head_dim
+
+
+def expanded_full_capacity_bytes(n_head: int, capacity: int, head_dim: int, elem: int) -> int:
+    """Logical K+V bytes of one layer when the KV heads are expanded to all
+    query heads and the whole capacity is consumed (the cost the active-prefix
+    slice removes)."""
+    return 2 * n_head * capacity * head_dim * elem
+
+
+def layers_for(kv_len: int, l2_bytes: int) -> int:
+    """Layer caches per kv_len so that their K+V total at least 3x L2."""
+    per_layer = 2 * N_KV_HEAD * kv_len * HEAD_DIM * ELEM
+    return max(2, math.ceil(3 * l2_bytes / per_layer))
+
+
+def measured_peaks() -> dict:
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            return json.loads(p.read_text())
+        except (OSError, ValueError):
+            pass
+    return {}
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling with nvidia-smi during the run.
+
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_id: str | None, period_ms: int = 100):
+        self.samples: list[list[str]] = []
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={CLOCK_QUERY}", "--format=csv,noheader,nounits", f"-lms={period_ms}"]
+        if gpu_id:
+            cmd.insert(1, f"--id={gpu_id}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append(parts)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in self.samples:
+            try:
+                sm.append(float(s[1]))
+                smax.append(float(s[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, s[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# The GPU arm.
+
+class SweepStep:
+    """Device state of one benchmark step and its CUDA-graph capture."""
+
+    def __init__(self, torch, da, device, seed: int, fused: bool):
+        self.torch, self.da, self.device, self.fused = torch, da, device, fused
+        props = torch.cuda.get_device_properties(device)
+        self.l2_bytes = int(props.L2_cache_size)
+        dt = torch.float16
+        self.groups = []
+        calls = []
+        for kv in SWEEP:
+            n_layers = layers_for(kv, self.l2_bytes)
+            gen = torch.Generator(device=device)
+            gen.manual_seed(seed * 1000003 + kv)
+            shape = (n_layers, B, N_KV_HEAD, kv, HEAD_DIM)
+            k = torch.empty(shape, dtype=dt, device=device)
+            v = torch.empty(shape, dtype=dt, device=device)
+            for t in (k, v):
+                for layer in range(n_layers):  # layer by layer keeps the fp32 temporary small
+                    t[layer].copy_(torch.randn(shape[1:], generator=gen, device=device, dtype=torch.float32))
+            self.groups.append({"kv_len": kv, "layers": n_layers, "k": k, "v": v})
+            calls += [(len(self.groups) - 1, layer) for layer in range(n_layers)]
+        self.calls = calls
+        n = len(calls)
+        # Per-step inputs packed in one buffer: [call, (q, k_new, v_new), B, heads, D] plus positions.
+        self.inputs = torch.empty((n, 3, B, N_HEAD, HEAD_DIM), dtype=dt, device=device)
+        gen = torch.Generator(device=device)
+        gen.manual_seed(seed * 7 + 1)
+        self.inputs.copy_(torch.randn(self.inputs.shape, generator=gen, device=device, dtype=torch.float32))
+        self.positions = torch.tensor([[self.groups[g]["kv_len"] - 1] for g, _ in calls], dtype=torch.int32,
+                                      device=device)
+        self.kv_lens = self.positions + 1
+        self.out = torch.empty((n, B, N_HEAD, HEAD_DIM), dtype=dt, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        ws = max(da.decode_attn_workspace_size(B, N_HEAD, N_KV_HEAD, HEAD_DIM, kv) for kv in SWEEP)
+        self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
+        self.splits = {kv: da.splits_for(B, N_HEAD, N_KV_HEAD, HEAD_DIM, kv, kv, dt) for kv in SWEEP}
+
+    # bytes -------------------------------------------------------------
+    def call_attend_bytes(self, i: int) -> int:
+        return attend_bytes(B, N_HEAD, N_KV_HEAD, HEAD_DIM, [self.groups[self.calls[i][0]]["kv_len"]])
+
+    def step_bytes(self) -> int:
+        return sum(self.call_attend_bytes(i) + append_bytes(B, N_KV_HEAD, HEAD_DIM) for i in range(len(self.calls)))
+
+    def launches_per_step(self) -> int:
+        n = 0
+        for g, _ in self.calls:
+            s = self.splits[self.groups[g]["kv_len"]]
+            n += (1 if self.fused else 2) + (1 if s > 1 else 0)
+        return n
+
+    # issue -------------------------------------------------------------
+    def issue(self, timing_events=None):
+        da = self.da
+        for i, (g, layer) in enumerate(self.calls):
+            grp = self.groups[g]
+            q, kn, vn = self.inputs[i, 0], self.inputs[i, 1], self.inputs[i, 2]
+            kc, vc = grp["k"][layer], grp["v"][layer]
+            if timing_events is not None:
+                da.set_timing_events(*timing_events[i])
+            if self.fused:
+                da.decode_step_fwd(q, kc, vc, kn, vn, self.positions[i], out=self.out[i], workspace=self.workspace,
+                                   max_kv_len_hint=grp["kv_len"], err_flag=self.err)
+            else:
+                da.kvcache_append(kc, vc, kn, vn, self.positions[i], err_flag=self.err)
+                da.decode_attn_fwd(q, kc, vc, self.kv_lens[i], out=self.out[i], workspace=self.workspace,
+                                   max_kv_len_hint=grp["kv_len"], err_flag=self.err)
+        if timing_events is not None:
+            da.set_timing_events(None, None)
+
+    def capture(self, timing_events=None):
+        torch = self.torch
+        s = torch.cuda.Stream(self.device)
+        s.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(s):
+            self.issue()  # eager warm-up: kernel attributes set before capture
+        torch.cuda.current_stream(self.device).wait_stream(s)
+        torch.cuda.synchronize(self.device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.issue(timing_events)
+        torch.cuda.synchronize(self.device)
+        return g
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+
+        if device is not None and str(device).startswith("cuda"):
+            dist.barrier(device_ids=[device.index if hasattr(device, "index") else 0])
+        else:
+            dist.barrier()
+
+
+def aggregate_value(bytes_per_rank_step: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job GB/s: the bytes all ranks processed over the slowest rank's time."""
+    return world * bytes_per_rank_step * steps / (max_ms * 1e-3) / 1e9
+
+
+def traffic_from_profiles(source_hash: str) -> dict | None:
+    """ncu DRAM traffic per decode-kernel launch recorded under profiles/, if
+    it was taken on the current kernel sources."""
+    p = ROOT / "profiles" / "decode_split_kernel_mha_sweep.md"
+    if not p.exists():
+        return None
+    rec = {}
+    for line in p.read_text().splitlines():
+        if line.startswith("- ") and ":" in line:
+            k, _, v = line[2:].partition(":")
+            rec[k.strip()] = v.strip().strip("`")
+    if rec.get("kernel_source_sha256") != source_hash:
+        return None
+    try:
+        return {kv: float(rec[f"traffic_bytes_kv{kv}"]) for kv in SWEEP}
+    except (KeyError, ValueError):
+        return None
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in sorted((ROOT / "decode_attention_static_gb300" / "csrc").glob("*")):
+        h.update(f.name.encode())
+        h.update(f.read_bytes())
+    return h.hexdigest()[:16]
+
+
+def run_ours(args) -> dict | None:
+    import torch
+
+    import decode_attention_static_gb300 as da
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device for the GPU arm")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=device)
+    da.build_library()
+    da.load_library()
+
+    step = SweepStep(torch, da, device, seed=args.seed + rank, fused=args.path == "fused")
+    graph = step.capture()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize(device)
+    if int(step.err.item()) != 0:
+        raise RuntimeError(f"device error flag {int(step.err.item())}")
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:  # noqa: BLE001 - older torch: sample every GPU
+        uuid = None
+    clocks = ClockSampler(uuid)
+
+    # ---- timed region: exactly K steps ----
+    stream = torch.cuda.current_stream(device)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    t0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world, device)
+    ms = t0.elapsed_time(t1)
+    ms_max = max_over_ranks(ms, world, device)
+
+    # ---- decode-kernel timing: events recorded around each decode launch ----
+    n = len(step.calls)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    kgraph = step.capture(timing_events=evs)
+    per_call = [0.0] * n
+    reps = max(3, min(20, args.steps // 10))
+    for _ in range(reps):
+        kgraph.replay()
+        torch.cuda.synchronize(device)
+        for i, (a, b) in enumerate(evs):
+            per_call[i] += a.elapsed_time(b)
+    per_call = [x / reps for x in per_call]
+
+    # ---- end to end: per-step H2D of the inputs and D2H of the outputs ----
+    h_in = torch.empty(step.inputs.shape, dtype=step.inputs.dtype, pin_memory=True)
+    h_in.copy_(step.inputs)
+    h_pos = torch.empty(step.positions.shape, dtype=torch.int32, pin_memory=True)
+    h_pos.copy_(step.positions)
+    h_kv = torch.empty(step.kv_lens.shape, dtype=torch.int32, pin_memory=True)
+    h_kv.copy_(step.kv_lens)
+    h_out = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(max(1, args.warmup // 4)):
+        step.inputs.copy_(h_in, non_blocking=True)
+        graph.replay()
+        h_out.copy_(step.out, non_blocking=True)
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    wall0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step.inputs.copy_(h_in, non_blocking=True)
+        step.positions.copy_(h_pos, non_blocking=True)
+        step.kv_lens.copy_(h_kv, non_blocking=True)
+        graph.replay()
+        h_out.copy_(step.out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    wall_ms = (time.perf_counter() - wall0) * 1e3
+    e2e_ms = max(e0.elapsed_time(e1), wall_ms)
+    e2e_ms_max = max_over_ranks(e2e_ms, world, device)
+    clk = clocks.stop()
+    if int(step.err.item()) != 0:
+        raise RuntimeError(f"device error flag {int(step.err.item())}")
+
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+
+    bytes_step = step.step_bytes()
+    value = aggregate_value(bytes_step, args.steps, world, ms_max)
+    peaks = measured_peaks()
+    peak = float(peaks.get("hbm_gbs") or FALLBACK_HBM_GBS)
+    peak_src = "measured" if peaks.get("hbm_gbs") else "fallback"
+
+    sweep = []
+    per_kv_kernel_ms, per_kv_bytes = {}, {}
+    for gi, grp in enumerate(step.groups):
+        idx = [i for i, (g, _) in enumerate(step.calls) if g == gi]
+        kms = sum(per_call[i] for i in idx)
+        kb = sum(step.call_attend_bytes(i) for i in idx)
+        per_kv_kernel_ms[grp["kv_len"]] = kms / len(idx)
+        per_kv_bytes[grp["kv_len"]] = kb / len(idx)
+        sweep.append({"kv_len": grp["kv_len"], "layers": grp["layers"], "splits": step.splits[grp["kv_len"]],
+                      "decode_kernel_us": round(kms / len(idx) * 1e3, 3),
+                      "decode_kernel_gbs": round(kb / (kms * 1e-3) / 1e9, 1)})
+    # us per layer-step of the whole step, apportioned by the kernel-time share of each kv_len
+    total_kms = sum(per_call)
+    for rec in sweep:
+        idx = [i for i, (g, _) in enumerate(step.calls) if step.groups[g]["kv_len"] == rec["kv_len"]]
+        share = sum(per_call[i] for i in idx) / total_kms
+        rec["us_per_layer_step"] = round(ms / args.steps * share / len(idx) * 1e3, 3)
+
+    k_bytes = sum(step.call_attend_bytes(i) for i in range(n))
+    k_ms = sum(per_call)
+    achieved = k_bytes / (k_ms * 1e-3) / 1e9
+    traffic = traffic_from_profiles(kernel_source_hash())
+    traffic_per_launch = None
+    if traffic:
+        traffic_per_launch = sum(traffic[step.groups[g]["kv_len"]] for g, _ in step.calls) / n
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "path": "fused append+attend" if step.fused else "append, then attend",
+                   "layers_per_kv_len": {str(g["kv_len"]): g["layers"] for g in step.groups},
+                   "l2": f"inputs larger than L2: each kv_len's layer caches total >= 3x L2 ({step.l2_bytes} B)",
+                   "timing": "CUDA-graph replay of the public calls, CUDA events on the launching stream",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "bytes_per_step": bytes_step},
+        "pct_of_peak_hbm": round(100 * value / peak, 1),
+        "pct_of_nominal_hbm": round(100 * value / NOMINAL_HBM_GBS, 1),
+        "sweep": sweep,
+        "roofline": {"kernel": "decode_split_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": None if traffic_per_launch is None else round(traffic_per_launch),
+                     "algorithmic_bytes_per_launch": round(k_bytes / n),
+                     "avg_launch_us": round(k_ms / n * 1e3, 3)},
+        "e2e": {"value": round(aggregate_value(bytes_step, args.steps, world, e2e_ms_max), 1), "unit": UNIT,
+                "h2d_bytes_per_step": step.inputs.numel() * ELEM + 2 * step.positions.numel() * 4,
+                "d2h_bytes_per_step": step.out.numel() * ELEM,
+                "mode": "pinned H2D of every layer's q/k_new/v_new and positions, graph replay, D2H of outputs"},
+        "gpu_launches": step.launches_per_step() * args.steps,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# The CPU oracle (the baseline arm and the cpu_baseline leg).
+
+def cpu_sample(n_heads: int = N_HEAD, seed: int = 0):
+    """One layer-step per kv_len of the sweep on the host (first n_heads heads)."""
+    from decode_attention_static_gb300 import workloads as W
+
+    items = []
+    for kv in SWEEP:
+        s = W.mha_sweep(kv, seed=seed)
+        items.append({
+            "kv_len": kv,
+            "q": W.raw_bits(s.q[:, :n_heads]).copy(),
+            "k": W.raw_bits(s.k_cache[:, :n_heads]).copy(),
+            "v": W.raw_bits(s.v_cache[:, :n_heads]).copy(),
+            "k_new": W.raw_bits(s.k_new[:, :n_heads]).copy(),
+            "v_new": W.raw_bits(s.v_new[:, :n_heads]).copy(),
+            "pos": s.position_ids.numpy().copy(),
+        })
+    bytes_ = sum(attend_bytes(B, n_heads, n_heads, HEAD_DIM, [it["kv_len"]]) + append_bytes(B, n_heads, HEAD_DIM)
+                 for it in items)
+    return items, bytes_
+
+
+def oracle_pass(ora, items, n_heads: int, threads: int):
+    for it in items:
+        ora.kvcache_append(it["k"], it["v"], it["k_new"], it["v_new"], it["pos"])
+        ora.decode_attn(it["q"], it["k"], it["v"], it["pos"] + 1, n_heads, n_heads, "f16", threads=threads)
+
+
+def cpu_baseline(budget_s: float) -> dict:
+    import oracle
+
+    ora = oracle.default()
+    threads = min(os.cpu_count() or 1, N_HEAD)
+    items, bytes_ = cpu_sample()
+    oracle_pass(ora, items, N_HEAD, threads)  # warm
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        oracle_pass(ora, items, N_HEAD, threads)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": round(bytes_ * passes / el / 1e9, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{passes} pass(es) of one layer-step per kv_len in {{1024, 4096, 8192}} (16 heads, append "
+                      f"+ attend) in {el:.1f} s, fp64 C oracle, OpenMP over query heads"}
+
+
+def run_reference(args) -> dict | None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+
+    ora = oracle.default()
+    threads = min(os.cpu_count() or 1, N_HEAD)
+    # size the sample so that warmup + steps fit in about two minutes
+    items, bytes_ = cpu_sample()
+    t = time.perf_counter()
+    oracle_pass(ora, items, N_HEAD, threads)
+    full = time.perf_counter() - t
+    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+    n_heads = max(1, min(N_HEAD, int(N_HEAD * per_step_budget / max(full, 1e-9))))
+    items, bytes_ = cpu_sample(n_heads)
+    threads = min(threads, n_heads)
+    for _ in range(args.warmup):
+        oracle_pass(ora, items, n_heads, threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_pass(ora, items, n_heads, threads)
+    el = time.perf_counter() - t0
+    value = bytes_ * args.steps / el / 1e9
+    sample = (f"each step: one layer-step per kv_len in {{1024, 4096, 8192}} on {n_heads} of the 16 heads "
+              f"(append + attend), fp64 C oracle, {threads} OpenMP thread(s)")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample_heads": n_heads},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--path", choices=["two_call", "fused"], default="two_call")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,219 @@
+"""ctypes binding of libdecode_attn.so: argument marshalling only.
+
+Every function here takes torch tensors that already live on the GPU, checks
+that their shapes agree, and passes raw pointers, sizes and the current CUDA
+stream to the C entry point of the same name. All computation happens in the
+library's kernels. If the library has not been built, every call raises
+``LibraryNotBuilt`` — there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import pathlib
+
+import torch
+
+LIBRARY = pathlib.Path(__file__).resolve().parent / "libdecode_attn.so"
+
+DA_F16 = 0
+DA_BF16 = 1
+DA_DEVERR_KV_LEN = 1
+DA_DEVERR_POSITION = 2
+DA_DEVERR_TIMEOUT = 4
+
+_DTYPE_CODE = {torch.float16: DA_F16, torch.bfloat16: DA_BF16}
+
+
+class LibraryNotBuilt(RuntimeError):
+    pass
+
+
+class DecodeAttnError(RuntimeError):
+    def __init__(self, fn: str, status: int, message: str):
+        super().__init__(f"{fn} failed with status {status}: {message}")
+        self.status = status
+
+
+_lib = None
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_SIGNATURES = {
+    "da_status_string": ([_i], ctypes.c_char_p),
+    "da_version": ([], _i),
+    "decode_attn_plan_splits": ([_i, _i, _i, _i, _i, _i], _i),
+    "decode_attn_workspace_size": ([_i, _i, _i, _i, _i], ctypes.c_size_t),
+    "decode_attn_splits_for": ([_i, _i, _i, _i, _i, _i, _i], _i),
+    "da_set_timing_events": ([_vp, _vp], _i),
+    "kvcache_append": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp], _i),
+    "decode_attn_fwd": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _vp, ctypes.c_size_t, _i, _i,
+                         _vp, _vp], _i),
+    "decode_step_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _vp, ctypes.c_size_t,
+                         _i, _i, _vp, _vp], _i),
+}
+
+
+def library_path() -> pathlib.Path:
+    return LIBRARY
+
+
+def load_library() -> ctypes.CDLL:
+    """Load the CUDA library (once). Raises LibraryNotBuilt if it is missing."""
+    global _lib
+    if _lib is None:
+        if not LIBRARY.exists():
+            raise LibraryNotBuilt(f"{LIBRARY} is missing: build it with decode_attention_static_gb300.build")
+        lib = ctypes.CDLL(str(LIBRARY))
+        for name, (args, res) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+    return _lib
+
+
+def exported_symbols() -> list[str]:
+    return list(_SIGNATURES)
+
+
+def status_string(status: int) -> str:
+    return load_library().da_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise DecodeAttnError(fn, status, status_string(status))
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(t: torch.Tensor) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in _DTYPE_CODE:
+        raise TypeError(f"dtype {t.dtype} is not supported (float16 or bfloat16)")
+    return _DTYPE_CODE[t.dtype]
+
+
+def _require(cond: bool, msg: str) -> None:
+    if not cond:
+        raise ValueError(msg)
+
+
+def _cuda_contig(name: str, t: torch.Tensor) -> None:
+    _require(t.is_cuda, f"{name} must be a CUDA tensor")
+    _require(t.is_contiguous(), f"{name} must be contiguous")
+
+
+def plan_splits(B: int, n_kv_head: int, head_dim: int, max_kv_len: int, num_sms: int, ctas_per_sm: int) -> int:
+    s = load_library().decode_attn_plan_splits(B, n_kv_head, head_dim, max_kv_len, num_sms, ctas_per_sm)
+    _check("decode_attn_plan_splits", s if s < 0 else 0)
+    return s
+
+
+def decode_attn_workspace_size(B: int, n_head: int, n_kv_head: int, head_dim: int, capacity: int) -> int:
+    n = load_library().decode_attn_workspace_size(B, n_head, n_kv_head, head_dim, capacity)
+    if n == ctypes.c_size_t(-1).value:
+        raise DecodeAttnError("decode_attn_workspace_size", -2, "invalid sizes or device query failed")
+    return int(n)
+
+
+def alloc_workspace(B: int, n_head: int, n_kv_head: int, head_dim: int, capacity: int, device=None) -> torch.Tensor:
+    """A device byte buffer of decode_attn_workspace_size() bytes (torch owns it)."""
+    n = decode_attn_workspace_size(B, n_head, n_kv_head, head_dim, capacity)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def splits_for(B: int, n_head: int, n_kv_head: int, head_dim: int, capacity: int, max_kv_len_hint: int = 0,
+               dtype: torch.dtype = torch.bfloat16) -> int:
+    """The split count decode_attn_fwd will use for these sizes on the current device."""
+    s = load_library().decode_attn_splits_for(B, n_head, n_kv_head, head_dim, capacity, int(max_kv_len_hint),
+                                              _DTYPE_CODE[dtype])
+    _check("decode_attn_splits_for", s if s < 0 else 0)
+    return s
+
+
+def set_timing_events(before: "torch.cuda.Event | None", after: "torch.cuda.Event | None") -> None:
+    """Record `before`/`after` around the decode kernel of every later call on
+    this thread (both None turns it off). Events need timing enabled."""
+    if before is None or after is None:
+        load_library().da_set_timing_events(None, None)
+        return
+    load_library().da_set_timing_events(ctypes.c_void_p(before.cuda_event), ctypes.c_void_p(after.cuda_event))
+
+
+def kvcache_append(k_cache: torch.Tensor, v_cache: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                   position_ids: torch.Tensor, err_flag: torch.Tensor | None = None) -> None:
+    """k_cache[b, g, position_ids[b]] = k_new[b, g] (and V), in place."""
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache), ("k_new", k_new), ("v_new", v_new),
+                 ("position_ids", position_ids)):
+        _cuda_contig(n, t)
+    _require(k_cache.dim() == 4 and v_cache.shape == k_cache.shape, "caches must be [B, n_kv_head, capacity, D]")
+    B, Hkv, cap, D = k_cache.shape
+    _require(tuple(k_new.shape) == (B, Hkv, D) and v_new.shape == k_new.shape, "k_new/v_new must be [B, n_kv_head, D]")
+    _require(position_ids.dtype == torch.int32 and position_ids.numel() == B, "position_ids must be int32 [B]")
+    _require(k_new.dtype == k_cache.dtype == v_cache.dtype == v_new.dtype, "dtypes differ")
+    st = load_library().kvcache_append(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(position_ids),
+                                       B, Hkv, D, cap, _dtype_code(k_cache), _ptr(err_flag), _stream(k_cache))
+    _check("kvcache_append", st)
+
+
+def _attn_shapes(q, k_cache, v_cache, out):
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("out", out)):
+        _cuda_contig(n, t)
+    _require(q.dim() == 3, "q must be [B, n_head, D]")
+    _require(k_cache.dim() == 4 and v_cache.shape == k_cache.shape, "caches must be [B, n_kv_head, capacity, D]")
+    B, H, D = q.shape
+    _require(k_cache.shape[0] == B and k_cache.shape[3] == D, "cache batch/head_dim must match q")
+    _require(out.shape == q.shape, "out must be [B, n_head, D]")
+    _require(q.dtype == k_cache.dtype == v_cache.dtype == out.dtype, "dtypes differ")
+    return B, H, k_cache.shape[1], D, k_cache.shape[2]
+
+
+def decode_attn_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, kv_len: torch.Tensor,
+                    out: torch.Tensor | None = None, scale: float | None = None,
+                    workspace: torch.Tensor | None = None, max_kv_len_hint: int = 0,
+                    err_flag: torch.Tensor | None = None) -> torch.Tensor:
+    """softmax(scale * q K[:kv_len]^T) V[:kv_len] per head; returns out [B, n_head, D]."""
+    if out is None:
+        out = torch.empty_like(q)
+    B, H, Hkv, D, cap = _attn_shapes(q, k_cache, v_cache, out)
+    _cuda_contig("kv_len", kv_len)
+    _require(kv_len.dtype == torch.int32 and kv_len.numel() == B, "kv_len must be int32 [B]")
+    if scale is None:
+        scale = D ** -0.5
+    if workspace is None:
+        workspace = alloc_workspace(B, H, Hkv, D, cap, q.device)
+    st = load_library().decode_attn_fwd(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), B, H, Hkv, D, cap,
+                                        float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
+                                        int(max_kv_len_hint), _dtype_code(q), _ptr(err_flag), _stream(q))
+    _check("decode_attn_fwd", st)
+    return out
+
+
+def decode_step_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, k_new: torch.Tensor,
+                    v_new: torch.Tensor, position_ids: torch.Tensor, out: torch.Tensor | None = None,
+                    scale: float | None = None, workspace: torch.Tensor | None = None, max_kv_len_hint: int = 0,
+                    err_flag: torch.Tensor | None = None) -> torch.Tensor:
+    """Fused append at position_ids then attention over [0, position_ids]."""
+    if out is None:
+        out = torch.empty_like(q)
+    B, H, Hkv, D, cap = _attn_shapes(q, k_cache, v_cache, out)
+    for n, t in (("k_new", k_new), ("v_new", v_new), ("position_ids", position_ids)):
+        _cuda_contig(n, t)
+    _require(tuple(k_new.shape) == (B, Hkv, D) and v_new.shape == k_new.shape, "k_new/v_new must be [B, n_kv_head, D]")
+    _require(position_ids.dtype == torch.int32 and position_ids.numel() == B, "position_ids must be int32 [B]")
+    if scale is None:
+        scale = D ** -0.5
+    if workspace is None:
+        workspace = alloc_workspace(B, H, Hkv, D, cap, q.device)
+    st = load_library().decode_step_fwd(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
+                                        _ptr(position_ids), B, H, Hkv, D, cap, float(scale), _ptr(out),
+                                        _ptr(workspace), workspace.numel(), int(max_kv_len_hint), _dtype_code(q),
+                                        _ptr(err_flag), _stream(q))
+    _check("decode_step_fwd", st)
+    return out

@@ -1,0 +1,278 @@
+// C ABI of the decode-attention library: argument validation, the split
+// plan, and the launches on the caller's stream. Nothing here allocates or
+// synchronises.
+#include <stdint.h>
+
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+
+#include "decode_attn.h"
+#include "launch.h"
+
+namespace da {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct DeviceState {
+  std::atomic<int> sms{0};
+  std::atomic<int> ready[2][2][4];  // [dtype][head_dim 64/128][log2 group]
+  DecodeKernelInfo info[2][2][4];
+};
+
+DeviceState g_devices[kMaxDevices];
+std::mutex g_mutex;
+
+int group_index(int group) { return group == 1 ? 0 : group == 2 ? 1 : group == 4 ? 2 : 3; }
+
+cudaError_t current_device(int* device) {
+  cudaError_t e = cudaGetDevice(device);
+  if (e != cudaSuccess) return e;
+  if (*device < 0 || *device >= kMaxDevices) return cudaErrorInvalidDevice;
+  return cudaSuccess;
+}
+
+cudaError_t device_sms(int device, int* sms) {
+  int n = g_devices[device].sms.load(std::memory_order_acquire);
+  if (n == 0) {
+    cudaError_t e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device);
+    if (e != cudaSuccess) return e;
+    g_devices[device].sms.store(n, std::memory_order_release);
+  }
+  *sms = n;
+  return cudaSuccess;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_sizes(int B, int n_head, int n_kv_head, int head_dim, int capacity, int dtype) {
+  if (dtype != DA_F16 && dtype != DA_BF16) return DA_ERR_DTYPE;
+  if (B < 0 || n_head < 1 || n_kv_head < 1 || head_dim < 1 || capacity < 1) return DA_ERR_SHAPE;
+  if (n_head % n_kv_head != 0) return DA_ERR_SHAPE;
+  if (B > 65535 || n_kv_head > 65535) return DA_ERR_SHAPE;  // grid z / y limits
+  if (!decode_supported(head_dim, n_head / n_kv_head)) return DA_ERR_UNSUPPORTED;
+  return DA_OK;
+}
+
+size_t workspace_bytes_for(int B, int n_head, int splits, int head_dim) {
+  if (splits <= 1) return 0;
+  const size_t rows = (size_t)B * n_head * splits;
+  return rows * head_dim * sizeof(float) + rows * 2 * sizeof(float);
+}
+
+}  // namespace
+
+bool decode_supported(int head_dim, int group) {
+  return (head_dim == 64 || head_dim == 128) && (group == 1 || group == 2 || group == 4 || group == 8);
+}
+
+cudaError_t decode_kernel_info(int dtype, int head_dim, int group, int device, DecodeKernelInfo* info) {
+  const int di = head_dim == 128 ? 1 : 0;
+  const int gi = group_index(group);
+  DeviceState& st = g_devices[device];
+  if (st.ready[dtype][di][gi].load(std::memory_order_acquire)) {
+    *info = st.info[dtype][di][gi];
+    return cudaSuccess;
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!st.ready[dtype][di][gi].load(std::memory_order_acquire)) {
+    DecodeKernelInfo k = {};
+    cudaError_t e = dtype == DA_F16 ? decode_info_f16(head_dim, group, &k) : decode_info_bf16(head_dim, group, &k);
+    if (e != cudaSuccess) return e;
+    if (k.ctas_per_sm < 1) return cudaErrorInvalidConfiguration;
+    st.info[dtype][di][gi] = k;
+    st.ready[dtype][di][gi].store(1, std::memory_order_release);
+  }
+  *info = st.info[dtype][di][gi];
+  return cudaSuccess;
+}
+
+cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int group, cudaStream_t stream) {
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  return dtype == DA_F16 ? launch_decode_f16(p, head_dim, group, stream, &attr)
+                         : launch_decode_bf16(p, head_dim, group, stream, &attr);
+}
+
+namespace {
+
+// Profiling hook events of this host thread (see da_set_timing_events).
+thread_local cudaEvent_t t_event_before = nullptr;
+thread_local cudaEvent_t t_event_after = nullptr;
+
+cudaError_t record_event(cudaEvent_t ev, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cs);
+  if (e != cudaSuccess) return e;
+  if (cs == cudaStreamCaptureStatusActive) return cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+  return cudaEventRecord(ev, st);
+}
+
+// Splits for the current device: plan + occupancy of the instance.
+int plan_for_device(int dtype, int B, int n_kv_head, int head_dim, int group, int bound, int* splits) {
+  int device = 0, sms = 0;
+  if (current_device(&device) != cudaSuccess) return DA_ERR_CUDA;
+  if (device_sms(device, &sms) != cudaSuccess) return DA_ERR_CUDA;
+  DecodeKernelInfo info;
+  if (decode_kernel_info(dtype, head_dim, group, device, &info) != cudaSuccess) return DA_ERR_CUDA;
+  const int s = decode_attn_plan_splits(B, n_kv_head, head_dim, bound, sms, info.ctas_per_sm);
+  if (s < 1) return s;
+  *splits = s;
+  return DA_OK;
+}
+
+int decode_common(const void* q, const void* k_cache, const void* v_cache, void* k_cache_w, void* v_cache_w,
+                  const void* k_new, const void* v_new, const int32_t* lens, int lens_are_positions, int B,
+                  int n_head, int n_kv_head, int head_dim, int capacity, float scale, void* out, void* workspace,
+                  size_t workspace_bytes, int max_kv_len_hint, int dtype, int32_t* err_flag, void* stream) {
+  int rc = check_sizes(B, n_head, n_kv_head, head_dim, capacity, dtype);
+  if (rc != DA_OK) return rc;
+  if (B == 0) return DA_OK;
+  if (!q || !k_cache || !v_cache || !lens || !out) return DA_ERR_NULL;
+  if (lens_are_positions && (!k_new || !v_new)) return DA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (k_new && !aligned16(k_new)) || (v_new && !aligned16(v_new)))
+    return DA_ERR_ALIGN;
+  const int group = n_head / n_kv_head;
+  const int bound = max_kv_len_hint > 0 ? std::min(max_kv_len_hint, capacity) : capacity;
+  int splits = 1;
+  rc = plan_for_device(dtype, B, n_kv_head, head_dim, group, bound, &splits);
+  if (rc != DA_OK) return rc;
+  const size_t need = workspace_bytes_for(B, n_head, splits, head_dim);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need) return DA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return DA_ERR_ALIGN;
+  }
+
+  DecodeParams p = {};
+  p.q = static_cast<const uint8_t*>(q);
+  p.k_cache = static_cast<const uint8_t*>(k_cache);
+  p.v_cache = static_cast<const uint8_t*>(v_cache);
+  p.k_cache_w = static_cast<uint8_t*>(k_cache_w);
+  p.v_cache_w = static_cast<uint8_t*>(v_cache_w);
+  p.k_new = static_cast<const uint8_t*>(k_new);
+  p.v_new = static_cast<const uint8_t*>(v_new);
+  p.lens = lens;
+  p.lens_are_positions = lens_are_positions;
+  p.B = B;
+  p.n_head = n_head;
+  p.n_kv_head = n_kv_head;
+  p.capacity = capacity;
+  p.splits = splits;
+  p.qscale = scale * kLog2e;
+  p.out = static_cast<uint8_t*>(out);
+  p.ws_acc = static_cast<float*>(workspace);
+  p.ws_ml = need > 0 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                                (size_t)B * n_head * splits * head_dim * sizeof(float))
+                     : nullptr;
+  p.err_flag = err_flag;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (t_event_before && record_event(t_event_before, st) != cudaSuccess) return DA_ERR_CUDA;
+  if (launch_decode(p, dtype, head_dim, group, st) != cudaSuccess) return DA_ERR_CUDA;
+  if (t_event_after && record_event(t_event_after, st) != cudaSuccess) return DA_ERR_CUDA;
+  if (splits > 1 && launch_combine(p, dtype, head_dim, st) != cudaSuccess) return DA_ERR_CUDA;
+  return DA_OK;
+}
+
+}  // namespace
+}  // namespace da
+
+extern "C" {
+
+const char* da_status_string(int status) {
+  switch (status) {
+    case DA_OK: return "ok";
+    case DA_ERR_NULL: return "a required pointer is NULL";
+    case DA_ERR_SHAPE: return "a size is out of range or inconsistent";
+    case DA_ERR_UNSUPPORTED: return "unsupported head_dim or group size (head_dim in {64,128}, group in {1,2,4,8})";
+    case DA_ERR_WORKSPACE: return "workspace is NULL or smaller than decode_attn_workspace_size()";
+    case DA_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
+    case DA_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case DA_ERR_DTYPE: return "unknown dtype code";
+    default: return "unknown status";
+  }
+}
+
+int da_version(void) { return 100; }
+
+int decode_attn_plan_splits(int B, int n_kv_head, int head_dim, int max_kv_len, int num_sms, int ctas_per_sm) {
+  if (B < 1 || n_kv_head < 1 || max_kv_len < 1 || num_sms < 1 || ctas_per_sm < 1) return DA_ERR_SHAPE;
+  if (head_dim != 64 && head_dim != 128) return DA_ERR_UNSUPPORTED;
+  const int64_t units = (int64_t)B * n_kv_head;
+  const int64_t target = (int64_t)num_sms * ctas_per_sm;
+  int64_t s = (target + units - 1) / units;
+  const int rows = da::tile_rows(head_dim);
+  const int64_t tiles = ((int64_t)max_kv_len + rows - 1) / rows;
+  s = std::min<int64_t>(s, tiles);
+  s = std::min<int64_t>(s, da::kMaxSplits);
+  return (int)std::max<int64_t>(s, 1);
+}
+
+size_t decode_attn_workspace_size(int B, int n_head, int n_kv_head, int head_dim, int capacity) {
+  if (da::check_sizes(B, n_head, n_kv_head, head_dim, capacity, DA_F16) != DA_OK) return (size_t)-1;
+  if (B == 0) return 0;
+  size_t most = 0;
+  for (int dtype = DA_F16; dtype <= DA_BF16; ++dtype) {
+    int splits = 1;
+    if (da::plan_for_device(dtype, B, n_kv_head, head_dim, n_head / n_kv_head, capacity, &splits) != DA_OK)
+      return (size_t)-1;
+    most = std::max(most, da::workspace_bytes_for(B, n_head, splits, head_dim));
+  }
+  return most;
+}
+
+int decode_attn_splits_for(int B, int n_head, int n_kv_head, int head_dim, int capacity, int max_kv_len_hint,
+                           int dtype) {
+  int rc = da::check_sizes(B, n_head, n_kv_head, head_dim, capacity, dtype);
+  if (rc != DA_OK) return rc;
+  if (B == 0) return 1;
+  const int bound = max_kv_len_hint > 0 ? std::min(max_kv_len_hint, capacity) : capacity;
+  int splits = 1;
+  rc = da::plan_for_device(dtype, B, n_kv_head, head_dim, n_head / n_kv_head, bound, &splits);
+  return rc != DA_OK ? rc : splits;
+}
+
+int da_set_timing_events(void* event_before, void* event_after) {
+  const bool on = event_before && event_after;
+  da::t_event_before = on ? static_cast<cudaEvent_t>(event_before) : nullptr;
+  da::t_event_after = on ? static_cast<cudaEvent_t>(event_after) : nullptr;
+  return DA_OK;
+}
+
+int kvcache_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new, const int32_t* position_ids,
+                   int B, int n_kv_head, int head_dim, int capacity, int dtype, int32_t* err_flag, void* stream) {
+  if (dtype != DA_F16 && dtype != DA_BF16) return DA_ERR_DTYPE;
+  if (B < 0 || n_kv_head < 1 || capacity < 1 || head_dim < 8 || head_dim % 8 != 0) return DA_ERR_SHAPE;
+  if (B == 0) return DA_OK;
+  if (!k_cache || !v_cache || !k_new || !v_new || !position_ids) return DA_ERR_NULL;
+  if (!da::aligned16(k_cache) || !da::aligned16(v_cache) || !da::aligned16(k_new) || !da::aligned16(v_new))
+    return DA_ERR_ALIGN;
+  if (da::launch_append(k_cache, v_cache, k_new, v_new, position_ids, B, n_kv_head, head_dim, capacity, err_flag,
+                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return DA_ERR_CUDA;
+  return DA_OK;
+}
+
+int decode_attn_fwd(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_len, int B, int n_head,
+                    int n_kv_head, int head_dim, int capacity, float scale, void* out, void* workspace,
+                    size_t workspace_bytes, int max_kv_len_hint, int dtype, int32_t* err_flag, void* stream) {
+  return da::decode_common(q, k_cache, v_cache, nullptr, nullptr, nullptr, nullptr, kv_len, 0, B, n_head, n_kv_head,
+                           head_dim, capacity, scale, out, workspace, workspace_bytes, max_kv_len_hint, dtype,
+                           err_flag, stream);
+}
+
+int decode_step_fwd(const void* q, void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                    const int32_t* position_ids, int B, int n_head, int n_kv_head, int head_dim, int capacity,
+                    float scale, void* out, void* workspace, size_t workspace_bytes, int max_kv_len_hint, int dtype,
+                    int32_t* err_flag, void* stream) {
+  return da::decode_common(q, k_cache, v_cache, k_cache, v_cache, k_new, v_new, position_ids, 1, B, n_head,
+                           n_kv_head, head_dim, capacity, scale, out, workspace, workspace_bytes, max_kv_len_hint,
+                           dtype, err_flag, stream);
+}
+
+}  // extern "C"

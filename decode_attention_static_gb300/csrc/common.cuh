@@ -1,0 +1,217 @@
+// Shared device helpers of the decode-attention library (sm_103a).
+//
+// Inline PTX wrappers for the mbarrier / bulk-copy (TMA) pipeline, the
+// programmatic-dependent-launch controls, fp16/bf16 <-> fp32 conversion and
+// the split geometry shared by the decode and combine kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace da {
+
+// Bits of the device error word (mirrors DA_DEVERR_* of the public header).
+constexpr int32_t kErrKvLen = 1;
+constexpr int32_t kErrPosition = 2;
+constexpr int32_t kErrTimeout = 4;
+
+// A pipeline wait gives up after this long and reports kErrTimeout.
+constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+
+// Decode kernel geometry. One stage holds kTileBytes of K rows and as many
+// bytes of V rows; kConsumerWarps warps compute, one more warp issues the
+// bulk copies.
+constexpr int kTileBytes = 8192;
+constexpr int kStages = 4;
+constexpr int kConsumerWarps = 4;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kDecodeThreads = kConsumerThreads + 32;
+constexpr int kMaxSplits = 128;
+
+__host__ __device__ constexpr int tile_rows(int head_dim) { return kTileBytes / (2 * head_dim); }
+
+// Rows per split for a sequence of L active rows cut into at most S splits:
+// an even share rounded up to whole tiles.
+__host__ __device__ inline int split_chunk(int L, int S, int rows_per_tile) {
+  const int share = (L + S - 1) / S;
+  return ((share + rows_per_tile - 1) / rows_per_tile) * rows_per_tile;
+}
+
+__host__ __device__ inline int active_splits(int L, int chunk) { return (L + chunk - 1) / chunk; }
+
+// ---------------------------------------------------------------------------
+// PTX wrappers.
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of the given parity to complete; false after
+// kWaitLimitNs without completion.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+// L2 policy for data streamed once.
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Bulk (non-tensor) TMA copy global -> shared, completing on `bar`.
+// Both addresses 16-byte aligned, bytes a positive multiple of 16.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(smem_addr(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+// Programmatic dependent launch: wait for the preceding grid's memory, and
+// allow the following grid to be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_addr(p)));
+  return v;
+}
+
+__device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// Storage types.
+
+template <typename T>
+struct Storage;
+
+template <>
+struct Storage<__nv_bfloat16> {
+  // 8 packed bf16 -> fp32 (exact: bf16 is the top half of an fp32).
+  static __device__ __forceinline__ void unpack(const uint4& v, float (&f)[8]) {
+    f[0] = __uint_as_float(v.x << 16);
+    f[1] = __uint_as_float(v.x & 0xffff0000u);
+    f[2] = __uint_as_float(v.y << 16);
+    f[3] = __uint_as_float(v.y & 0xffff0000u);
+    f[4] = __uint_as_float(v.z << 16);
+    f[5] = __uint_as_float(v.z & 0xffff0000u);
+    f[6] = __uint_as_float(v.w << 16);
+    f[7] = __uint_as_float(v.w & 0xffff0000u);
+  }
+  static __device__ __forceinline__ uint16_t round(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
+  static constexpr uint16_t kNaN = 0x7FC0;
+};
+
+template <>
+struct Storage<__half> {
+  static __device__ __forceinline__ float2 pair(uint32_t u) {
+    __half2 h = *reinterpret_cast<__half2*>(&u);
+    return __half22float2(h);
+  }
+  static __device__ __forceinline__ void unpack(const uint4& v, float (&f)[8]) {
+    float2 a = pair(v.x), b = pair(v.y), c = pair(v.z), d = pair(v.w);
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+  }
+  static __device__ __forceinline__ uint16_t round(float x) { return __half_as_ushort(__float2half_rn(x)); }
+  static constexpr uint16_t kNaN = 0x7E00;
+};
+
+// Parameters shared by the decode and combine kernels.
+struct DecodeParams {
+  const uint8_t* q;        // [B, n_head, D]
+  const uint8_t* k_cache;  // [B, n_kv_head, capacity, D]
+  const uint8_t* v_cache;
+  uint8_t* k_cache_w;      // fused step: caches to write the new row into (else null)
+  uint8_t* v_cache_w;
+  const uint8_t* k_new;    // fused step: [B, n_kv_head, D] (else null)
+  const uint8_t* v_new;
+  const int32_t* lens;     // kv_len, or position_ids when lens_are_positions
+  int lens_are_positions;
+  int B, n_head, n_kv_head, capacity, splits;
+  float qscale;            // softmax scale * log2(e)
+  uint8_t* out;            // [B, n_head, D]
+  float* ws_acc;           // [B, n_head, splits, D]
+  float* ws_ml;            // [B, n_head, splits, 2]: running max (log2 units), sum
+  int32_t* err_flag;       // may be null
+};
+
+// Active length of sequence b, or -1 when its input is out of range
+// (setting the matching error bit in *err).
+__device__ __forceinline__ int sequence_length(const DecodeParams& p, int b, int32_t* err_bits) {
+  const int v = p.lens[b];
+  if (p.lens_are_positions) {
+    if (v < 0 || v >= p.capacity) {
+      *err_bits = kErrPosition | kErrKvLen;
+      return -1;
+    }
+    return v + 1;
+  }
+  if (v < 1 || v > p.capacity) {
+    *err_bits = kErrKvLen;
+    return -1;
+  }
+  return v;
+}
+
+}  // namespace da

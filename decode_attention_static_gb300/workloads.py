@@ -60,8 +60,7 @@ def randn(shape, dtype, gen: torch.Generator) -> torch.Tensor:
 def nan_like(shape, dtype, device="cpu") -> torch.Tensor:
     """A tensor of the dtype's canonical quiet NaN."""
     dt = torch_dtype(dtype)
-    bits = torch.full(shape, NAN_BITS[dt], dtype=torch.int32, device=device).to(torch.int16)
-    return bits.view(dt)
+    return torch.full(shape, NAN_BITS[dt], dtype=torch.int16, device=device).view(dt)
 
 
 def raw_bits(t: torch.Tensor):

@@ -1,0 +1,169 @@
+/*
+ * decode_attn.h — C ABI of the GB300 (sm_103a) decode-attention library.
+ *
+ * One autoregressive decode step of one attention layer over a STATIC,
+ * preallocated KV cache: the new key/value row is written in place at
+ * position_id, and a single query token per head attends to the active prefix
+ * [0, kv_len) of the cache only, with kv_len = position_id + 1. Grouped-query
+ * heads are served straight from their shared KV head (no expansion).
+ *
+ * The operation follows:
+ *  - VoxCPM issue #395, "MiniCPM4 MiniCPMAttention.forward_step Attention
+ *    Performance Fix", section 3 (attend to the slice [0, position_id] only;
+ *    position 0 attends to one row and returns V[0]) and section 4.1 (the
+ *    patched forward_step: in-place write key_cache[:, :, position_id, :],
+ *    then SDPA on the slice with enable_gqa=True);
+ *  - fish-speech issue #1310, "Optimize native AR decoding by attending only
+ *    to the active KV-cache prefix", section 2 (the cache keeps its physical
+ *    max_seq_len size; only k[:, :, :kv_len], v[:, :, :kv_len] are consumed);
+ *  - Cuda-Compute-OSS issue #343, "one-token decode fast path", section
+ *    "Proposed implementation" (softmax(q K^T / sqrt(d)) V, max-subtracted
+ *    softmax accumulated in fp32, result cast back to the input dtype).
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers to contiguous row-major arrays
+ *    owned by the caller, 16-byte aligned. The library never allocates,
+ *    frees or synchronises; work is enqueued on `stream` (a cudaStream_t;
+ *    NULL is the legacy default stream) and the call returns at once.
+ *  - Layouts: q and out [B, n_head, head_dim]; k_cache and v_cache
+ *    [B, n_kv_head, capacity, head_dim]; k_new and v_new
+ *    [B, n_kv_head, head_dim]; kv_len and position_ids int32 [B].
+ *    Query head h reads KV head h / (n_head / n_kv_head).
+ *  - dtype is DA_F16 or DA_BF16 and applies to q, out and both caches.
+ *    Arithmetic is fp32; out is rounded to nearest even.
+ *  - Supported: head_dim in {64, 128}; n_head / n_kv_head in {1, 2, 4, 8}.
+ *  - Errors the host can see (null pointers, bad sizes, misalignment, a
+ *    small workspace, an unsupported shape) return a negative da_status
+ *    before anything is enqueued. Facts only the device knows (a kv_len
+ *    outside [1, capacity], a position outside [0, capacity)) never fault:
+ *    the affected output rows become NaN, the affected cache write is
+ *    skipped, and the DA_DEVERR_* bit is OR-ed into *err_flag (a device
+ *    int32, may be NULL). A launch failure returns DA_ERR_CUDA.
+ */
+#ifndef DECODE_ATTN_H_
+#define DECODE_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DA_API __attribute__((visibility("default")))
+#else
+#define DA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { DA_F16 = 0, DA_BF16 = 1 } da_dtype;
+
+typedef enum {
+  DA_OK = 0,
+  DA_ERR_NULL = -1,        /* a required pointer is NULL */
+  DA_ERR_SHAPE = -2,       /* a size is out of range or inconsistent */
+  DA_ERR_UNSUPPORTED = -3, /* valid but not built: head_dim or group size */
+  DA_ERR_WORKSPACE = -4,   /* workspace NULL or smaller than required */
+  DA_ERR_CUDA = -5,        /* a CUDA runtime call or launch failed */
+  DA_ERR_ALIGN = -6,       /* a pointer is not 16-byte aligned */
+  DA_ERR_DTYPE = -7        /* unknown dtype code */
+} da_status;
+
+/* Bits OR-ed into *err_flag by the kernels. */
+#define DA_DEVERR_KV_LEN 1u   /* some kv_len[b] outside [1, capacity]: rows of b are NaN */
+#define DA_DEVERR_POSITION 2u /* some position_ids[b] outside [0, capacity): write skipped */
+#define DA_DEVERR_TIMEOUT 4u  /* a pipeline wait hit its time limit: rows are NaN */
+
+/* Human-readable name of a da_status value (static string). */
+DA_API const char* da_status_string(int status);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+DA_API int da_version(void);
+
+/*
+ * Split plan of the decode kernel, a pure host computation (no CUDA call):
+ * the number of KV splits S per (sequence, KV head) for B sequences,
+ * n_kv_head KV heads, head_dim, a bound on the active length max_kv_len, and
+ * a GPU with num_sms multiprocessors running ctas_per_sm decode CTAs each.
+ * Each sequence b then splits its own kv_len[b] rows evenly over at most S
+ * CTAs, in whole tiles. Returns S >= 1, or a negative da_status.
+ */
+DA_API int decode_attn_plan_splits(int B, int n_kv_head, int head_dim, int max_kv_len, int num_sms,
+                            int ctas_per_sm);
+
+/*
+ * Bytes of scratch memory decode_attn_fwd / decode_step_fwd need for these
+ * sizes on the current device, for any max_kv_len_hint <= capacity.
+ * Returns 0 when no scratch is needed, or (size_t)-1 for invalid sizes or a
+ * failed device query. The workspace holds fp32 partial results
+ * [B, n_head, S, head_dim + 2]; it needs no initialisation.
+ */
+DA_API size_t decode_attn_workspace_size(int B, int n_head, int n_kv_head, int head_dim, int capacity);
+
+/*
+ * The split count S that decode_attn_fwd / decode_step_fwd will use for
+ * these arguments on the current device (1 means a single launch that writes
+ * out directly; S > 1 adds the combine launch and needs the workspace).
+ * Returns S >= 1 or a negative da_status.
+ */
+DA_API int decode_attn_splits_for(int B, int n_head, int n_kv_head, int head_dim, int capacity,
+                                  int max_kv_len_hint, int dtype);
+
+/*
+ * Profiling hook. When both are non-NULL, every later decode_attn_fwd /
+ * decode_step_fwd call made by this host thread records event_before (a
+ * cudaEvent_t) on its stream immediately before its split-KV decode kernel
+ * and event_after immediately after it, so that cudaEventElapsedTime gives
+ * that kernel's device time. Under stream capture the records become graph
+ * nodes. NULL, NULL turns the hook off. Returns DA_OK.
+ */
+DA_API int da_set_timing_events(void* event_before, void* event_after);
+
+/*
+ * In-place append: k_cache[b, g, position_ids[b], :] = k_new[b, g, :] and the
+ * same for V, for every sequence b and KV head g, copied bit for bit.
+ * (VoxCPM issue #395, section 4.1.) A position outside [0, capacity) skips
+ * that sequence and sets DA_DEVERR_POSITION.
+ */
+DA_API int kvcache_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                   const int32_t* position_ids, int B, int n_kv_head, int head_dim, int capacity,
+                   int dtype, int32_t* err_flag, void* stream);
+
+/*
+ * Decode attention over the active prefix:
+ *   out[b, h, :] = softmax_j(scale * <q[b, h, :], K[b, g, j, :]>) V[b, g, j, :]
+ * for j in [0, kv_len[b]) and g = h / (n_head / n_kv_head). Cache rows at or
+ * beyond kv_len[b] are never read. kv_len is a DEVICE array, so no host
+ * synchronisation is needed; max_kv_len_hint (> 0) is an optional host bound
+ * on max_b kv_len[b] that only sizes the launch (<= 0 means capacity). A
+ * kv_len above the hint but within capacity is still computed correctly.
+ * workspace/workspace_bytes: caller-owned device scratch of at least
+ * decode_attn_workspace_size(...) bytes (may be NULL when that is 0); calls
+ * that share one workspace must not overlap on the GPU.
+ * (Cuda-Compute-OSS issue #343, "Proposed implementation"; VoxCPM issue
+ * #395, section 4.1.)
+ */
+DA_API int decode_attn_fwd(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_len,
+                    int B, int n_head, int n_kv_head, int head_dim, int capacity, float scale,
+                    void* out, void* workspace, size_t workspace_bytes, int max_kv_len_hint,
+                    int dtype, int32_t* err_flag, void* stream);
+
+/*
+ * One fused decode step: the append of kvcache_append followed by
+ * decode_attn_fwd with kv_len[b] = position_ids[b] + 1, in a single pass
+ * over the cache. The attended row position_ids[b] is taken from k_new/v_new
+ * and also written into the cache. Same arguments, layouts and error
+ * behaviour as the two calls it replaces (VoxCPM issue #395, section 4.1:
+ * write at position_id, then attend over [0, position_id]).
+ */
+DA_API int decode_step_fwd(const void* q, void* k_cache, void* v_cache, const void* k_new,
+                    const void* v_new, const int32_t* position_ids, int B, int n_head,
+                    int n_kv_head, int head_dim, int capacity, float scale, void* out,
+                    void* workspace, size_t workspace_bytes, int max_kv_len_hint, int dtype,
+                    int32_t* err_flag, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DECODE_ATTN_H_ */

@@ -1,0 +1,139 @@
+"""The C ABI on the host: the library loads, exports every symbol the header
+declares, and rejects bad arguments before touching the GPU (CPU only; no
+compute call is made)."""
+import ctypes
+import pathlib
+import re
+import subprocess
+
+import pytest
+import torch
+
+import decode_attention_static_gb300 as da
+from decode_attention_static_gb300 import build as da_build
+
+ROOT = pathlib.Path(__file__).resolve().parents[1]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    da_build.build_library()
+    return da.load_library()
+
+
+def declared_symbols():
+    names = set()
+    for h in (ROOT / "include").glob("*.h"):
+        text = h.read_text()
+        names |= set(re.findall(r"^DA_API\s+[\w\s\*]+?\b(\w+)\s*\(", text, flags=re.M))
+    return names
+
+
+def test_header_declares_entry_points():
+    names = declared_symbols()
+    assert {"kvcache_append", "decode_attn_fwd", "decode_step_fwd", "decode_attn_workspace_size",
+            "decode_attn_plan_splits", "da_status_string", "da_version"} <= names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", str(da.library_path())], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    missing = declared_symbols() - exported
+    assert not missing, f"declared but not exported: {missing}"
+    for name in declared_symbols():
+        assert getattr(lib, name) is not None
+    assert declared_symbols() <= set(da.exported_symbols()), "binding lacks a declared entry point"
+
+
+def test_status_strings(lib):
+    for code in range(-7, 1):
+        assert da.status_string(code) not in ("", "unknown status")
+    assert da.status_string(-99) == "unknown status"
+
+
+def test_plan_splits_properties(lib):
+    sms, per = 152, 3
+    # one (b, kv-head) unit per CTA already fills the GPU: no split
+    assert da.plan_splits(64, 8, 128, 32768, sms, per) == 1
+    # long context, 8 units: enough splits for a full wave
+    s = da.plan_splits(1, 8, 128, 32768, sms, per)
+    assert s * 8 >= sms * per and s <= 128
+    # never more splits than 32-row tiles (D=128) or 64-row tiles (D=64)
+    assert da.plan_splits(1, 1, 128, 40, sms, per) == 2
+    assert da.plan_splits(1, 1, 64, 40, sms, per) == 1
+    assert da.plan_splits(1, 1, 128, 1, sms, per) == 1
+    # monotone in the length bound, so a workspace sized for capacity fits any hint
+    prev = 0
+    for n in range(1, 9000, 37):
+        cur = da.plan_splits(1, 16, 128, n, sms, per)
+        assert cur >= prev
+        prev = cur
+    for bad in [(0, 8, 128, 10, sms, per), (1, 0, 128, 10, sms, per), (1, 8, 128, 0, sms, per),
+                (1, 8, 128, 10, 0, per), (1, 8, 128, 10, sms, 0)]:
+        assert lib.decode_attn_plan_splits(*bad) == -2
+    assert lib.decode_attn_plan_splits(1, 8, 96, 10, sms, per) == -3
+
+
+A = 0x10000  # a 16-byte-aligned address that is never dereferenced by these calls
+
+
+def _fwd(lib, **kw):
+    args = dict(q=A, k=A, v=A, kv_len=A, B=1, H=32, Hkv=8, D=128, cap=1024, scale=0.1, out=A, ws=A, ws_bytes=1 << 30,
+                hint=0, dtype=1, err=None, stream=None)
+    args.update(kw)
+    return lib.decode_attn_fwd(args["q"], args["k"], args["v"], args["kv_len"], args["B"], args["H"], args["Hkv"],
+                               args["D"], args["cap"], args["scale"], args["out"], args["ws"], args["ws_bytes"],
+                               args["hint"], args["dtype"], args["err"], args["stream"])
+
+
+def test_decode_attn_fwd_rejects_bad_arguments(lib):
+    assert _fwd(lib, dtype=2) == -7
+    assert _fwd(lib, dtype=-1) == -7
+    assert _fwd(lib, H=30) == -2          # n_head not a multiple of n_kv_head
+    assert _fwd(lib, B=-1) == -2
+    assert _fwd(lib, cap=0) == -2
+    assert _fwd(lib, Hkv=0) == -2
+    assert _fwd(lib, B=70000) == -2
+    assert _fwd(lib, D=96) == -3
+    assert _fwd(lib, D=256) == -3
+    assert _fwd(lib, H=24, Hkv=8) == -3   # group 3 not built
+    assert _fwd(lib, H=128, Hkv=8) == -3  # group 16 not built
+    assert _fwd(lib, q=None) == -1
+    assert _fwd(lib, kv_len=None) == -1
+    assert _fwd(lib, out=None) == -1
+    assert _fwd(lib, q=A + 8) == -6
+    assert _fwd(lib, out=A + 2) == -6
+    assert _fwd(lib, B=0, q=None, k=None) == 0  # empty batch: nothing to do
+
+
+def test_decode_step_and_append_reject_bad_arguments(lib):
+    st = lib.decode_step_fwd(A, A, A, None, A, A, 1, 32, 8, 128, 1024, 0.1, A, A, 1 << 30, 0, 1, None, None)
+    assert st == -1
+    st = lib.decode_step_fwd(A, A, A, A, A + 4, A, 1, 32, 8, 128, 1024, 0.1, A, A, 1 << 30, 0, 1, None, None)
+    assert st == -6
+    assert lib.kvcache_append(A, A, A, A, A, 1, 8, 128, 1024, 5, None, None) == -7
+    assert lib.kvcache_append(A, A, A, A, A, 1, 8, 12, 1024, 1, None, None) == -2
+    assert lib.kvcache_append(A, A, A, A, A, 1, 8, 128, 0, 1, None, None) == -2
+    assert lib.kvcache_append(A, None, A, A, A, 1, 8, 128, 1024, 1, None, None) == -1
+    assert lib.kvcache_append(A, A, A + 1, A, A, 1, 8, 128, 1024, 1, None, None) == -6
+    assert lib.kvcache_append(None, None, None, None, None, 0, 8, 128, 1024, 1, None, None) == 0
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
+def test_valid_call_without_gpu_reports_cuda_error(lib):
+    assert _fwd(lib) == -5
+    assert lib.decode_attn_workspace_size(1, 32, 8, 128, 1024) == ctypes.c_size_t(-1).value
+
+
+def test_workspace_size_rejects_bad_sizes(lib):
+    assert lib.decode_attn_workspace_size(1, 30, 8, 128, 1024) == ctypes.c_size_t(-1).value
+    assert lib.decode_attn_workspace_size(1, 32, 8, 100, 1024) == ctypes.c_size_t(-1).value
+    assert lib.decode_attn_workspace_size(0, 32, 8, 128, 1024) == 0
+
+
+def test_binding_checks_tensor_arguments():
+    cpu = torch.zeros(1, 4, 64, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        da.decode_attn_fwd(cpu, torch.zeros(1, 1, 8, 64, dtype=torch.float16),
+                           torch.zeros(1, 1, 8, 64, dtype=torch.float16), torch.ones(1, dtype=torch.int32))

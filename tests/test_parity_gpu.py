@@ -1,0 +1,247 @@
+"""GPU parity: the CUDA library through its C ABI against the fp64 oracle on
+the seeded synthetic workloads, at full size, plus edge cases. Tolerances:
+rel-Frobenius <= 5e-3 and max-abs <= 2e-2 for the attention output; the
+cache append is compared bit for bit, NaN tail included."""
+import numpy as np
+import pytest
+import torch
+
+import decode_attention_static_gb300 as da
+from decode_attention_static_gb300 import workloads as W
+from gpu_helpers import THREADS, assert_close, bits, check_step, gpu_step, oracle_step
+
+pytestmark = pytest.mark.gpu
+
+FUSED = [False, True]
+FUSED_IDS = ["append+attend", "fused_step"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    da.build_library()
+    da.load_library()
+
+
+@pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
+def test_tiny_gqa(ora, fused):
+    check_step(ora, W.tiny_gqa(seed=0), fused, what="tiny GQA")
+
+
+@pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
+@pytest.mark.parametrize("kv_len", W.MHA_SWEEP_KV_LENS)
+def test_mha_sweep(ora, kv_len, fused):
+    check_step(ora, W.mha_sweep(kv_len, seed=1), fused, what=f"MHA kv {kv_len}")
+
+
+@pytest.mark.parametrize("kv_len", W.MHA_SWEEP_KV_LENS)
+def test_mha_sweep_nan_tail(ora, kv_len):
+    check_step(ora, W.mha_sweep(kv_len, seed=2, extra_capacity=64), False, what=f"MHA kv {kv_len} + tail")
+
+
+@pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
+def test_long_context(ora, fused):
+    check_step(ora, W.long_context(seed=3), fused, what="long context 32768")
+
+
+@pytest.mark.parametrize("seed", [4, 5])
+@pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
+def test_batched_streaming(ora, fused, seed):
+    step = W.batched_streaming(seed=seed)
+    assert int(step.position_ids.min()) == 0
+    check_step(ora, step, fused, what="batched streaming")
+
+
+@pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
+def test_s2pro_generation(ora, fused):
+    """36 layers x 400 steps of append + attend; every 50th step (and the
+    last) checked against the oracle in every layer; final caches bit-exact."""
+    g = W.s2pro_generation(seed=6)
+    dev = "cuda"
+    shape = (g.layers, g.B, g.n_kv_head, g.capacity, g.head_dim)
+    kc = W.nan_like(shape, g.dtype, device=dev)
+    vc = W.nan_like(shape, g.dtype, device=dev)
+    kc[:, :, :, :g.prompt] = g.k_prefix.to(dev)
+    vc[:, :, :, :g.prompt] = g.v_prefix.to(dev)
+    q, kn, vn = g.q.to(dev), g.k_new.to(dev), g.v_new.to(dev)
+    check_steps = sorted(set(range(0, g.steps, 50)) | {g.steps - 1})
+    outs = {}
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = da.alloc_workspace(g.B, g.n_head, g.n_kv_head, g.head_dim, g.capacity)
+    for i in range(g.steps):
+        pos = torch.full((g.B,), g.position(i), dtype=torch.int32, device=dev)
+        kv = pos + 1
+        for layer in range(g.layers):
+            if fused:
+                o = da.decode_step_fwd(q[i, layer], kc[layer], vc[layer], kn[i, layer], vn[i, layer], pos,
+                                       workspace=ws, max_kv_len_hint=g.position(i) + 1, err_flag=err)
+            else:
+                da.kvcache_append(kc[layer], vc[layer], kn[i, layer], vn[i, layer], pos, err_flag=err)
+                o = da.decode_attn_fwd(q[i, layer], kc[layer], vc[layer], kv, workspace=ws,
+                                       max_kv_len_hint=g.position(i) + 1, err_flag=err)
+            if i in check_steps:
+                outs[(i, layer)] = o.clone()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    end = g.prompt + g.steps
+    k_full = torch.cat([g.k_prefix, g.k_new.permute(1, 2, 3, 0, 4)], dim=3)  # [layers, B, Hkv, end, D]
+    v_full = torch.cat([g.v_prefix, g.v_new.permute(1, 2, 3, 0, 4)], dim=3)
+    assert np.array_equal(bits(kc[:, :, :, :end]), bits(k_full)), "K cache prefix"
+    assert np.array_equal(bits(vc[:, :, :, :end]), bits(v_full)), "V cache prefix"
+    assert bool(torch.isnan(kc[:, :, :, end:].float()).all()) and bool(torch.isnan(vc[:, :, :, end:].float()).all())
+    for (i, layer), o in outs.items():
+        L = g.position(i) + 1
+        ref = ora.decode_attn(bits(g.q[i, layer]), bits(k_full[layer]), bits(v_full[layer]),
+                              np.array([L], np.int32), g.n_head, g.n_kv_head, g.dtype, threads=THREADS)
+        assert_close(o, ref, f"step {i} layer {layer}")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("D,H,Hkv", [(64, 4, 1), (128, 16, 16), (128, 32, 8), (64, 16, 8), (128, 8, 1), (64, 8, 8)])
+def test_position_zero_returns_v0_bit_exact(dtype, D, H, Hkv):
+    """kv_len 1 -> softmax over one entry -> out = V[0], bit for bit."""
+    step = W.decode_step(3, H, Hkv, D, 300, dtype, [0, 0, 0], seed=7)
+    for fused in FUSED:
+        d, out, err = gpu_step(step, fused)
+        assert err == 0
+        G = H // Hkv
+        v0 = d.v_cache[:, :, 0, :].repeat_interleave(G, dim=1)
+        assert torch.equal(out.view(torch.int16), v0.contiguous().view(torch.int16))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_edge_lengths(ora, dtype, D, G):
+    """Lengths at and around tile and split boundaries, ragged across the
+    batch, with a NaN tail; both call styles."""
+    tile = 8192 // (2 * D)
+    Hkv = 2
+    lens = [1, 2, tile - 1, tile, tile + 1, 2 * tile + 3, 1000, 1531]
+    cap = max(lens) + 7
+    pos = [L - 1 for L in lens]
+    step = W.decode_step(len(lens), G * Hkv, Hkv, D, cap, dtype, pos, seed=D * 10 + G)
+    for fused in FUSED:
+        check_step(ora, step, fused, what=f"{dtype} D{D} G{G} fused={fused}")
+
+
+def test_capacity_one_and_full(ora):
+    check_step(ora, W.decode_step(2, 8, 2, 128, 1, "bf16", [0, 0], seed=8), True, what="capacity 1")
+    check_step(ora, W.decode_step(2, 8, 2, 64, 777, "f16", [776, 776], seed=9), False, what="full capacity")
+
+
+@pytest.mark.parametrize("hint", [1, 64, 5000, 100000])
+def test_hint_only_sizes_the_launch(ora, hint):
+    """Any max_kv_len_hint gives the same correct result, even one below the
+    real lengths."""
+    step = W.decode_step(2, 32, 8, 128, 4096, "bf16", [4095, 1200], seed=10)
+    check_step(ora, step, False, hint=hint, what=f"hint {hint}")
+    check_step(ora, step, True, hint=hint, what=f"fused hint {hint}")
+
+
+def test_fused_step_matches_two_calls_bitwise():
+    step = W.batched_streaming(seed=11)
+    d1, o1, e1 = gpu_step(step, False)
+    d2, o2, e2 = gpu_step(step, True)
+    assert e1 == e2 == 0
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(d1.k_cache.view(torch.int16), d2.k_cache.view(torch.int16))
+    assert torch.equal(d1.v_cache.view(torch.int16), d2.v_cache.view(torch.int16))
+
+
+def test_deterministic():
+    step = W.long_context(seed=12, kv_len=20000)
+    outs = [gpu_step(step, False)[1] for _ in range(3)]
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+
+
+def test_empty_batch():
+    q = torch.empty(0, 8, 128, dtype=torch.bfloat16, device="cuda")
+    kc = torch.empty(0, 2, 16, 128, dtype=torch.bfloat16, device="cuda")
+    kv = torch.empty(0, dtype=torch.int32, device="cuda")
+    out = da.decode_attn_fwd(q, kc, kc.clone(), kv)
+    assert out.shape == (0, 8, 128)
+
+
+def test_invalid_lengths_give_nan_rows_and_error_bits(ora):
+    step = W.decode_step(3, 8, 2, 128, 100, "f16", [50, 5, 50], seed=13)
+    d = step.to("cuda")
+    kv_len = torch.tensor([0, 6, 101], dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = da.decode_attn_fwd(d.q, d.k_cache, d.v_cache, kv_len, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == da.DA_DEVERR_KV_LEN
+    assert bool(torch.isnan(out[0].float()).all()) and bool(torch.isnan(out[2].float()).all())
+    ref = ora.decode_attn(bits(step.q[1:2]), bits(step.k_cache[1:2]), bits(step.v_cache[1:2]),
+                          np.array([5], np.int32), 8, 2, "f16")
+    # row 5 is NaN in the input (it is the append slot); kv_len 6 reads it
+    assert np.all(np.isnan(ref))
+    kv_len = torch.tensor([0, 5, 101], dtype=torch.int32, device="cuda")
+    err.zero_()
+    out = da.decode_attn_fwd(d.q, d.k_cache, d.v_cache, kv_len, err_flag=err)
+    ref = ora.decode_attn(bits(step.q[1:2]), bits(step.k_cache[1:2]), bits(step.v_cache[1:2]),
+                          np.array([5], np.int32), 8, 2, "f16")
+    assert_close(out[1:2], ref, "valid row among invalid ones")
+    assert int(err.item()) == da.DA_DEVERR_KV_LEN
+
+
+def test_invalid_positions_skip_the_write(ora):
+    step = W.decode_step(3, 8, 2, 64, 40, "bf16", [10, 3, 10], seed=14)
+    for fused in FUSED:
+        d = step.to("cuda")
+        before_k = d.k_cache.clone()
+        pos = torch.tensor([-1, 3, 40], dtype=torch.int32, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        if fused:
+            out = da.decode_step_fwd(d.q, d.k_cache, d.v_cache, d.k_new, d.v_new, pos, err_flag=err)
+        else:
+            da.kvcache_append(d.k_cache, d.v_cache, d.k_new, d.v_new, pos, err_flag=err)
+            out = None
+        torch.cuda.synchronize()
+        expect = da.DA_DEVERR_POSITION | (da.DA_DEVERR_KV_LEN if fused else 0)
+        assert int(err.item()) == expect
+        assert torch.equal(d.k_cache[0].view(torch.int16), before_k[0].view(torch.int16))
+        assert torch.equal(d.k_cache[2].view(torch.int16), before_k[2].view(torch.int16))
+        assert torch.equal(d.k_cache[1, :, 3].view(torch.int16), d.k_new[1].view(torch.int16))
+        if fused:
+            assert bool(torch.isnan(out[0].float()).all()) and bool(torch.isnan(out[2].float()).all())
+            assert bool(torch.isfinite(out[1].float()).all())
+
+
+def test_no_writes_outside_out_and_workspace():
+    step = W.long_context(seed=15, kv_len=9000, capacity=9000)
+    d = step.to("cuda")
+    B, H, D = d.q.shape
+    guard = 64
+    out_buf = torch.full((B * H * D + 2 * guard,), 12345, dtype=torch.int16, device="cuda")
+    out = out_buf[guard:guard + B * H * D].view(torch.bfloat16).view(B, H, D)
+    n = da.decode_attn_workspace_size(B, H, 8, D, d.capacity)
+    assert n > 0
+    ws_buf = torch.full((n + 2 * 256,), 7, dtype=torch.uint8, device="cuda")
+    ws = ws_buf[256:256 + n]
+    da.kvcache_append(d.k_cache, d.v_cache, d.k_new, d.v_new, d.position_ids)
+    da.decode_attn_fwd(d.q, d.k_cache, d.v_cache, d.kv_len.contiguous(), out=out, workspace=ws)
+    torch.cuda.synchronize()
+    assert bool((out_buf[:guard] == 12345).all()) and bool((out_buf[-guard:] == 12345).all())
+    assert bool((ws_buf[:256] == 7).all()) and bool((ws_buf[-256:] == 7).all())
+
+
+def test_side_stream(ora):
+    step = W.decode_step(2, 16, 8, 128, 3000, "bf16", [2999, 17], seed=16)
+    kb, vb, ref = oracle_step(ora, step)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        d = step.to("cuda")
+        out = da.decode_step_fwd(d.q, d.k_cache, d.v_cache, d.k_new, d.v_new, d.position_ids)
+    s.synchronize()
+    assert_close(out, ref, "side stream")
+
+
+def test_small_workspace_is_rejected():
+    step = W.long_context(seed=17, kv_len=4096, capacity=4096).to("cuda")
+    with pytest.raises(da.DecodeAttnError) as e:
+        da.decode_attn_fwd(step.q, step.k_cache, step.v_cache, step.kv_len.contiguous(),
+                           workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == -4
