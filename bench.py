@@ -337,6 +337,10 @@ def run_ours(args) -> dict | None:
     # ---- decode-kernel timing: events recorded around each decode launch ----
     n = len(step.calls)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in evs:  # torch creates the CUDA event on its first record
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize(device)
     kgraph = step.capture(timing_events=evs)
     per_call = [0.0] * n
     reps = max(3, min(20, args.steps // 10))

@@ -174,10 +174,11 @@ def test_invalid_lengths_give_nan_rows_and_error_bits(ora):
     torch.cuda.synchronize()
     assert int(err.item()) == da.DA_DEVERR_KV_LEN
     assert bool(torch.isnan(out[0].float()).all()) and bool(torch.isnan(out[2].float()).all())
+    # kv_len 6 of sequence 1 includes its NaN row 5 (the unwritten append
+    # slot): a NaN inside the prefix propagates on both sides
     ref = ora.decode_attn(bits(step.q[1:2]), bits(step.k_cache[1:2]), bits(step.v_cache[1:2]),
-                          np.array([5], np.int32), 8, 2, "f16")
-    # row 5 is NaN in the input (it is the append slot); kv_len 6 reads it
-    assert np.all(np.isnan(ref))
+                          np.array([6], np.int32), 8, 2, "f16")
+    assert np.all(np.isnan(ref)) and bool(torch.isnan(out[1].float()).all())
     kv_len = torch.tensor([0, 5, 101], dtype=torch.int32, device="cuda")
     err.zero_()
     out = da.decode_attn_fwd(d.q, d.k_cache, d.v_cache, kv_len, err_flag=err)
