@@ -15,6 +15,8 @@ from ._binding import (  # noqa: F401
     LibraryNotBuilt,
     alloc_workspace,
     decode_attn_fwd,
+    decode_attn_fwd_static_scratch,
+    STATIC_SCRATCH_BYTES,
     decode_attn_workspace_size,
     decode_step_fwd,
     exported_symbols,

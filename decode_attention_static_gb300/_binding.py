@@ -48,6 +48,8 @@ _SIGNATURES = {
     "kvcache_append": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp], _i),
     "decode_attn_fwd": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _vp, ctypes.c_size_t, _i, _i,
                          _vp, _vp], _i),
+    "decode_attn_fwd_static_scratch": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _i, _i, _vp,
+                                        _vp], _i),
     "decode_step_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _vp, ctypes.c_size_t,
                          _i, _i, _vp, _vp], _i),
 }
@@ -216,4 +218,29 @@ def decode_step_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
                                         _ptr(workspace), workspace.numel(), int(max_kv_len_hint), _dtype_code(q),
                                         _ptr(err_flag), _stream(q))
     _check("decode_step_fwd", st)
+    return out
+
+
+STATIC_SCRATCH_BYTES = 1 << 20  # DA_STATIC_SCRATCH_BYTES of the C header
+
+
+def decode_attn_fwd_static_scratch(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                   kv_len: torch.Tensor, out: torch.Tensor | None = None,
+                                   scale: float | None = None, max_kv_len_hint: int = 0,
+                                   err_flag: torch.Tensor | None = None) -> torch.Tensor:
+    """decode_attn_fwd without a caller workspace: the library's own fixed
+    device scratch array holds the split partials (for callers that may not
+    allocate GPU memory). ``out`` must be given by such callers; when it is
+    None this helper creates it with torch for convenience."""
+    if out is None:
+        out = torch.empty_like(q)
+    B, H, Hkv, D, cap = _attn_shapes(q, k_cache, v_cache, out)
+    _cuda_contig("kv_len", kv_len)
+    _require(kv_len.dtype == torch.int32 and kv_len.numel() == B, "kv_len must be int32 [B]")
+    if scale is None:
+        scale = D ** -0.5
+    st = load_library().decode_attn_fwd_static_scratch(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), B, H,
+                                                       Hkv, D, cap, float(scale), _ptr(out), int(max_kv_len_hint),
+                                                       _dtype_code(q), _ptr(err_flag), _stream(q))
+    _check("decode_attn_fwd_static_scratch", st)
     return out

@@ -162,6 +162,43 @@ DA_API int decode_step_fwd(const void* q, void* k_cache, void* v_cache, const vo
                     void* workspace, size_t workspace_bytes, int max_kv_len_hint, int dtype,
                     int32_t* err_flag, void* stream);
 
+/* Size of the library-owned scratch array used by
+ * decode_attn_fwd_static_scratch (1 MiB per GPU that loads the library). */
+#define DA_STATIC_SCRATCH_BYTES (1u << 20)
+
+/*
+ * decode_attn_fwd for callers that must not allocate GPU memory. This entry
+ * point is an addition of this library; the pages have no counterpart.
+ *
+ * Some callers only receive input and output buffers from the framework that
+ * hosts them (a plugin inside an inference server or a real-time audio
+ * engine, for instance) and are not allowed to call cudaMalloc, or cannot
+ * reach the memory pool that owns the device memory. This variant takes the
+ * same arguments as decode_attn_fwd minus the workspace: its split partials
+ * live in a file-scope device array of DA_STATIC_SCRATCH_BYTES that the
+ * library holds on every GPU that loads it, until the process exits. Nothing
+ * is allocated or freed by the call.
+ *
+ * - The first call on a device looks up that array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture on the device.
+ * - Arguments whose split plan needs more scratch than
+ *   DA_STATIC_SCRATCH_BYTES (decode_attn_workspace_size-style need for this
+ *   call's max_kv_len_hint) are rejected with DA_ERR_SHAPE before anything is
+ *   enqueued; use decode_attn_fwd with your own workspace for those.
+ * - Every call on a device shares the one array and leaves its partials in
+ *   it. The kernels write every partial they later read, so nothing needs to
+ *   start at zero, but calls that overlap on the GPU (different streams
+ *   without ordering, or different host threads) race on the array and give
+ *   wrong results: keep such calls ordered.
+ * Otherwise identical to decode_attn_fwd, including results bit for bit.
+ */
+DA_API int decode_attn_fwd_static_scratch(const void* q, const void* k_cache, const void* v_cache,
+                                          const int32_t* kv_len, int B, int n_head, int n_kv_head,
+                                          int head_dim, int capacity, float scale, void* out,
+                                          int max_kv_len_hint, int dtype, int32_t* err_flag,
+                                          void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,67 @@
+"""decode_attn_fwd_static_scratch: the entry point for callers that may not
+allocate GPU memory (for instance a plugin that only gets input and output
+buffers from the server or audio engine hosting it). Its split partials live
+in the library's own fixed device array instead of a caller workspace.
+
+The file name makes pytest collect it last, so a run that stops at the first
+failure has already run every other test."""
+import pytest
+import torch
+
+import decode_attention_static_gb300 as da
+from decode_attention_static_gb300 import workloads as W
+from gpu_helpers import assert_close, oracle_step
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    da.build_library()
+    da.load_library()
+
+
+def _scratch_need(step, hint):
+    s = da.splits_for(step.B, step.n_head, step.n_kv_head, step.head_dim, step.capacity, hint,
+                      W.torch_dtype(step.dtype))
+    return s, (step.B * step.n_head * s * (step.head_dim + 2) * 4 if s > 1 else 0)
+
+
+def test_matches_workspace_entry_point_on_two_calls_in_a_row(ora):
+    """Two different decode steps back to back through the no-allocation entry
+    point: each matches decode_attn_fwd (with a caller workspace) and the
+    fp64 oracle, so the second call does not see the first call's partials."""
+    steps = [W.long_context(seed=21, kv_len=30001), W.batched_streaming(seed=22)]
+    for step in steps:
+        splits, need = _scratch_need(step, 0)
+        assert splits > 1 and 0 < need <= da.STATIC_SCRATCH_BYTES  # the scratch path is exercised
+    outs = []
+    for step in steps:
+        d = step.to("cuda")
+        da.kvcache_append(d.k_cache, d.v_cache, d.k_new, d.v_new, d.position_ids)
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        got = da.decode_attn_fwd_static_scratch(d.q, d.k_cache, d.v_cache, d.kv_len.contiguous(), err_flag=err)
+        ref = da.decode_attn_fwd(d.q, d.k_cache, d.v_cache, d.kv_len.contiguous())
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert_close(got, ref.double().cpu().numpy(), "static scratch vs workspace entry point")
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+        outs.append((step, got.clone()))
+    for step, got in outs:
+        _, _, oref = oracle_step(ora, step)
+        assert_close(got, oref, "static scratch vs oracle")
+
+
+def test_rejects_sizes_beyond_the_scratch_limit():
+    # 15 sequences x 10 KV heads x 8 query heads each: at least two splits on
+    # a 152-SM GPU, so the partials need >= 15*80*2*130*4 B > 1 MiB
+    step = W.decode_step(15, 80, 10, 128, 64, "bf16", [63] * 15, seed=23)
+    splits, need = _scratch_need(step, 0)
+    d = step.to("cuda")
+    if need <= da.STATIC_SCRATCH_BYTES:
+        pytest.skip("this GPU's split plan fits the scratch array")
+    with pytest.raises(da.DecodeAttnError) as e:
+        da.decode_attn_fwd_static_scratch(d.q, d.k_cache, d.v_cache, d.kv_len.contiguous())
+    assert e.value.status == -2
