@@ -1,5 +1,5 @@
 #!/usr/bin/env python
-"""Benchmark of the decode-attention hot path (append + split-KV decode + combine).
+"""Benchmark of the decode-attention hot path (append + split-KV decode with its merge).
 
 Workload: the MHA decode sweep — B=1, 16 query heads on 16 KV heads, head_dim
 128, fp16, kv_len in {1024, 4096, 8192} with capacity = kv_len. One step is
@@ -7,8 +7,9 @@ one decode token through every layer of a model whose layers each own a
 static cache: for each kv_len, `layers` caches (enough that the caches of one
 kv_len total at least 3x the L2 size, so every layer reads cold HBM), and for
 every layer an in-place append at kv_len - 1 followed by attention over the
-kv_len rows. The step is captured once in a CUDA graph from the public API
-calls and replayed; timing uses CUDA events on the launching stream.
+kv_len rows. The step's public API calls are captured once in CUDA graphs
+(one per kv_len) and replayed; timing uses CUDA events on the launching
+stream.
 
 Printed: one JSON line with the whole-job achieved HBM GB/s over algorithmic
 bytes (K/V prefix read once + q read + out write + the appended rows), the
@@ -143,14 +144,14 @@ class ClockSampler:
 class SweepStep:
     """Device state of one benchmark step and its CUDA-graph capture."""
 
-    def __init__(self, torch, da, device, seed: int, fused: bool):
+    def __init__(self, torch, da, device, seed: int, fused: bool, kv_lens=SWEEP):
         self.torch, self.da, self.device, self.fused = torch, da, device, fused
         props = torch.cuda.get_device_properties(device)
         self.l2_bytes = int(props.L2_cache_size)
         dt = torch.float16
         self.groups = []
         calls = []
-        for kv in SWEEP:
+        for kv in kv_lens:
             n_layers = layers_for(kv, self.l2_bytes)
             gen = torch.Generator(device=device)
             gen.manual_seed(seed * 1000003 + kv)
@@ -174,9 +175,10 @@ class SweepStep:
         self.kv_lens = self.positions + 1
         self.out = torch.empty((n, B, N_HEAD, HEAD_DIM), dtype=dt, device=device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
-        ws = max(da.decode_attn_workspace_size(B, N_HEAD, N_KV_HEAD, HEAD_DIM, kv) for kv in SWEEP)
+        ws = max(da.decode_attn_workspace_size(B, N_HEAD, N_KV_HEAD, HEAD_DIM, kv) for kv in kv_lens)
         self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
-        self.splits = {kv: da.splits_for(B, N_HEAD, N_KV_HEAD, HEAD_DIM, kv, kv, dt) for kv in SWEEP}
+        # (splits, cluster size) of each kv_len's calls
+        self.splits = {kv: da.splits_for(B, N_HEAD, N_KV_HEAD, HEAD_DIM, kv, kv, dt) for kv in kv_lens}
 
     # bytes -------------------------------------------------------------
     def call_attend_bytes(self, i: int) -> int:
@@ -186,16 +188,16 @@ class SweepStep:
         return sum(self.call_attend_bytes(i) + append_bytes(B, N_KV_HEAD, HEAD_DIM) for i in range(len(self.calls)))
 
     def launches_per_step(self) -> int:
-        n = 0
-        for g, _ in self.calls:
-            s = self.splits[self.groups[g]["kv_len"]]
-            n += (1 if self.fused else 2) + (1 if s > 1 else 0)
-        return n
+        # one decode launch per layer (the split merge runs inside it), plus
+        # the append launch unless the step is fused
+        return len(self.calls) * (1 if self.fused else 2)
 
     # issue -------------------------------------------------------------
-    def issue(self, timing_events=None):
+    def issue(self, timing_events=None, group=None):
         da = self.da
         for i, (g, layer) in enumerate(self.calls):
+            if group is not None and g != group:
+                continue
             grp = self.groups[g]
             q, kn, vn = self.inputs[i, 0], self.inputs[i, 1], self.inputs[i, 2]
             kc, vc = grp["k"][layer], grp["v"][layer]
@@ -211,19 +213,22 @@ class SweepStep:
         if timing_events is not None:
             da.set_timing_events(None, None)
 
-    def capture(self, timing_events=None):
+    def capture(self, timing_events=None, group=None):
         torch = self.torch
         s = torch.cuda.Stream(self.device)
         s.wait_stream(torch.cuda.current_stream(self.device))
         with torch.cuda.stream(s):
-            self.issue()  # eager warm-up: kernel attributes set before capture
+            self.issue(group=group)  # eager warm-up: kernel attributes set before capture
         torch.cuda.current_stream(self.device).wait_stream(s)
         torch.cuda.synchronize(self.device)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self.issue(timing_events)
+            self.issue(timing_events, group)
         torch.cuda.synchronize(self.device)
         return g
+
+    def group_calls(self, gi: int) -> list[int]:
+        return [i for i, (g, _) in enumerate(self.calls) if g == gi]
 
 
 def dist_env():
@@ -305,10 +310,16 @@ def run_ours(args) -> dict | None:
     da.build_library()
     da.load_library()
 
-    step = SweepStep(torch, da, device, seed=args.seed + rank, fused=args.path == "fused")
-    graph = step.capture()
+    kv_lens = tuple(int(x) for x in args.kv_lens.split(","))
+    step = SweepStep(torch, da, device, seed=args.seed + rank, fused=args.path == "fused", kv_lens=kv_lens)
+    graphs = [step.capture(group=gi) for gi in range(len(step.groups))]
+
+    def replay_step():
+        for g in graphs:
+            g.replay()
+
     for _ in range(args.warmup):
-        graph.replay()
+        replay_step()
     torch.cuda.synchronize(device)
     if int(step.err.item()) != 0:
         raise RuntimeError(f"device error flag {int(step.err.item())}")
@@ -327,29 +338,51 @@ def run_ours(args) -> dict | None:
     torch.cuda.synchronize(device)
     t0.record(stream)
     for _ in range(args.steps):
-        graph.replay()
+        replay_step()
     t1.record(stream)
     torch.cuda.synchronize(device)
     barrier(world, device)
     ms = t0.elapsed_time(t1)
     ms_max = max_over_ranks(ms, world, device)
 
-    # ---- decode-kernel timing: events recorded around each decode launch ----
-    n = len(step.calls)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-    for a, b in evs:  # torch creates the CUDA event on its first record
-        a.record(stream)
-        b.record(stream)
-    torch.cuda.synchronize(device)
-    kgraph = step.capture(timing_events=evs)
-    per_call = [0.0] * n
-    reps = max(3, min(20, args.steps // 10))
-    for _ in range(reps):
-        kgraph.replay()
+    # ---- us per layer-step for each kv_len: each group's graph timed alone ----
+    group_ms = []
+    for gi, g in enumerate(graphs):
+        g.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(device)
-        for i, (a, b) in enumerate(evs):
-            per_call[i] += a.elapsed_time(b)
-    per_call = [x / reps for x in per_call]
+        a.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        group_ms.append(a.elapsed_time(b) / args.steps)
+
+    # ---- decode-kernel launch duration ----
+    n = len(step.calls)
+    if step.fused:
+        # every launch of the timed region is a decode kernel: average duration
+        # = timed region / launches, per kv_len from the per-group timings
+        per_call = [group_ms[g] / step.groups[g]["layers"] for g, _ in step.calls]
+        kernel_timing = "timed region / decode launches (the fused step launches only the decode kernel)"
+    else:
+        # events the library records right before and after each decode launch
+        # (graph event nodes: includes the launch latency the nodes expose)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in evs:  # torch creates the CUDA event on its first record
+            a.record(stream)
+            b.record(stream)
+        torch.cuda.synchronize(device)
+        kgraph = step.capture(timing_events=evs)
+        per_call = [0.0] * n
+        reps = max(3, min(20, args.steps // 10))
+        for _ in range(reps):
+            kgraph.replay()
+            torch.cuda.synchronize(device)
+            for i, (a, b) in enumerate(evs):
+                per_call[i] += a.elapsed_time(b)
+        per_call = [x / reps for x in per_call]
+        kernel_timing = "events recorded by the library around each decode launch (upper bound)"
 
     # ---- end to end: per-step H2D of the inputs and D2H of the outputs ----
     h_in = torch.empty(step.inputs.shape, dtype=step.inputs.dtype, pin_memory=True)
@@ -362,7 +395,7 @@ def run_ours(args) -> dict | None:
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for _ in range(max(1, args.warmup // 4)):
         step.inputs.copy_(h_in, non_blocking=True)
-        graph.replay()
+        replay_step()
         h_out.copy_(step.out, non_blocking=True)
     barrier(world, device)
     torch.cuda.synchronize(device)
@@ -372,7 +405,7 @@ def run_ours(args) -> dict | None:
         step.inputs.copy_(h_in, non_blocking=True)
         step.positions.copy_(h_pos, non_blocking=True)
         step.kv_lens.copy_(h_kv, non_blocking=True)
-        graph.replay()
+        replay_step()
         h_out.copy_(step.out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize(device)
@@ -397,22 +430,17 @@ def run_ours(args) -> dict | None:
     peak_src = "measured" if peaks.get("hbm_gbs") else "fallback"
 
     sweep = []
-    per_kv_kernel_ms, per_kv_bytes = {}, {}
     for gi, grp in enumerate(step.groups):
-        idx = [i for i, (g, _) in enumerate(step.calls) if g == gi]
+        idx = step.group_calls(gi)
         kms = sum(per_call[i] for i in idx)
         kb = sum(step.call_attend_bytes(i) for i in idx)
-        per_kv_kernel_ms[grp["kv_len"]] = kms / len(idx)
-        per_kv_bytes[grp["kv_len"]] = kb / len(idx)
-        sweep.append({"kv_len": grp["kv_len"], "layers": grp["layers"], "splits": step.splits[grp["kv_len"]],
+        step_b = sum(step.call_attend_bytes(i) + append_bytes(B, N_KV_HEAD, HEAD_DIM) for i in idx)
+        splits, cluster = step.splits[grp["kv_len"]]
+        sweep.append({"kv_len": grp["kv_len"], "layers": grp["layers"], "splits": splits, "cluster": cluster,
+                      "us_per_layer_step": round(group_ms[gi] / len(idx) * 1e3, 3),
+                      "gbs": round(step_b / (group_ms[gi] * 1e-3) / 1e9, 1),
                       "decode_kernel_us": round(kms / len(idx) * 1e3, 3),
                       "decode_kernel_gbs": round(kb / (kms * 1e-3) / 1e9, 1)})
-    # us per layer-step of the whole step, apportioned by the kernel-time share of each kv_len
-    total_kms = sum(per_call)
-    for rec in sweep:
-        idx = [i for i, (g, _) in enumerate(step.calls) if step.groups[g]["kv_len"] == rec["kv_len"]]
-        share = sum(per_call[i] for i in idx) / total_kms
-        rec["us_per_layer_step"] = round(ms / args.steps * share / len(idx) * 1e3, 3)
 
     k_bytes = sum(step.call_attend_bytes(i) for i in range(n))
     k_ms = sum(per_call)
@@ -426,10 +454,12 @@ def run_ours(args) -> dict | None:
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "path": "fused append+attend" if step.fused else "append, then attend",
+        "config": {"workload": WORKLOAD if kv_lens == SWEEP else f"{WORKLOAD} (subset kv_len {list(kv_lens)})",
+                   "path": "fused append+attend" if step.fused else "append, then attend",
                    "layers_per_kv_len": {str(g["kv_len"]): g["layers"] for g in step.groups},
                    "l2": f"inputs larger than L2: each kv_len's layer caches total >= 3x L2 ({step.l2_bytes} B)",
-                   "timing": "CUDA-graph replay of the public calls, CUDA events on the launching stream",
+                   "timing": "CUDA-graph replay of the public calls (one graph per kv_len), CUDA events on the "
+                             "launching stream",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "bytes_per_step": bytes_step},
         "pct_of_peak_hbm": round(100 * value / peak, 1),
@@ -439,7 +469,7 @@ def run_ours(args) -> dict | None:
                      "peak": peak, "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": None if traffic_per_launch is None else round(traffic_per_launch),
                      "algorithmic_bytes_per_launch": round(k_bytes / n),
-                     "avg_launch_us": round(k_ms / n * 1e3, 3)},
+                     "avg_launch_us": round(k_ms / n * 1e3, 3), "timing": kernel_timing},
         "e2e": {"value": round(aggregate_value(bytes_step, args.steps, world, e2e_ms_max), 1), "unit": UNIT,
                 "h2d_bytes_per_step": step.inputs.numel() * ELEM + 2 * step.positions.numel() * 4,
                 "d2h_bytes_per_step": step.out.numel() * ELEM,
@@ -544,8 +574,11 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--path", choices=["two_call", "fused"], default="two_call")
+    ap.add_argument("--path", choices=["two_call", "fused"], default="fused",
+                    help="fused: one decode_step_fwd per layer; two_call: kvcache_append then decode_attn_fwd")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--kv-lens", default=",".join(map(str, SWEEP)),
+                    help="kv_len values of the sweep to run (a subset gives a smaller case, e.g. for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

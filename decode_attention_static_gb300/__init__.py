@@ -10,6 +10,7 @@ from ._binding import (  # noqa: F401
     DA_DEVERR_KV_LEN,
     DA_DEVERR_POSITION,
     DA_DEVERR_TIMEOUT,
+    DA_DEVERR_WORKSPACE,
     DA_F16,
     DecodeAttnError,
     LibraryNotBuilt,
@@ -27,6 +28,7 @@ from ._binding import (  # noqa: F401
     set_timing_events,
     splits_for,
     status_string,
+    workspace_init,
 )
 
 

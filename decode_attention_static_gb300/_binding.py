@@ -20,6 +20,7 @@ DA_BF16 = 1
 DA_DEVERR_KV_LEN = 1
 DA_DEVERR_POSITION = 2
 DA_DEVERR_TIMEOUT = 4
+DA_DEVERR_WORKSPACE = 8
 
 _DTYPE_CODE = {torch.float16: DA_F16, torch.bfloat16: DA_BF16}
 
@@ -41,9 +42,10 @@ _i = ctypes.c_int
 _SIGNATURES = {
     "da_status_string": ([_i], ctypes.c_char_p),
     "da_version": ([], _i),
-    "decode_attn_plan_splits": ([_i, _i, _i, _i, _i, _i], _i),
+    "decode_attn_plan_splits": ([_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_i)], _i),
     "decode_attn_workspace_size": ([_i, _i, _i, _i, _i], ctypes.c_size_t),
-    "decode_attn_splits_for": ([_i, _i, _i, _i, _i, _i, _i], _i),
+    "decode_attn_workspace_init": ([_vp, ctypes.c_size_t, _vp], _i),
+    "decode_attn_splits_for": ([_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_i)], _i),
     "da_set_timing_events": ([_vp, _vp], _i),
     "kvcache_append": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp], _i),
     "decode_attn_fwd": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _vp, ctypes.c_size_t, _i, _i,
@@ -111,10 +113,14 @@ def _cuda_contig(name: str, t: torch.Tensor) -> None:
     _require(t.is_contiguous(), f"{name} must be contiguous")
 
 
-def plan_splits(B: int, n_kv_head: int, head_dim: int, max_kv_len: int, num_sms: int, ctas_per_sm: int) -> int:
-    s = load_library().decode_attn_plan_splits(B, n_kv_head, head_dim, max_kv_len, num_sms, ctas_per_sm)
+def plan_splits(B: int, n_kv_head: int, head_dim: int, max_kv_len: int, num_sms: int, ctas_per_sm: int,
+                cluster_max: int = 16) -> tuple[int, int]:
+    """(splits, cluster size) of the host split plan."""
+    cs = ctypes.c_int(0)
+    s = load_library().decode_attn_plan_splits(B, n_kv_head, head_dim, max_kv_len, num_sms, ctas_per_sm,
+                                               cluster_max, ctypes.byref(cs))
     _check("decode_attn_plan_splits", s if s < 0 else 0)
-    return s
+    return s, cs.value
 
 
 def decode_attn_workspace_size(B: int, n_head: int, n_kv_head: int, head_dim: int, capacity: int) -> int:
@@ -125,18 +131,26 @@ def decode_attn_workspace_size(B: int, n_head: int, n_kv_head: int, head_dim: in
 
 
 def alloc_workspace(B: int, n_head: int, n_kv_head: int, head_dim: int, capacity: int, device=None) -> torch.Tensor:
-    """A device byte buffer of decode_attn_workspace_size() bytes (torch owns it)."""
+    """A zero-filled device byte buffer of decode_attn_workspace_size() bytes (torch owns it)."""
     n = decode_attn_workspace_size(B, n_head, n_kv_head, head_dim, capacity)
-    return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def workspace_init(workspace: torch.Tensor) -> None:
+    """Zero-fill a workspace on the current stream (needed once before first use)."""
+    _cuda_contig("workspace", workspace)
+    st = load_library().decode_attn_workspace_init(_ptr(workspace), workspace.numel(), _stream(workspace))
+    _check("decode_attn_workspace_init", st)
 
 
 def splits_for(B: int, n_head: int, n_kv_head: int, head_dim: int, capacity: int, max_kv_len_hint: int = 0,
-               dtype: torch.dtype = torch.bfloat16) -> int:
-    """The split count decode_attn_fwd will use for these sizes on the current device."""
+               dtype: torch.dtype = torch.bfloat16) -> tuple[int, int]:
+    """(splits, cluster size) decode_attn_fwd will use for these sizes on the current device."""
+    cs = ctypes.c_int(0)
     s = load_library().decode_attn_splits_for(B, n_head, n_kv_head, head_dim, capacity, int(max_kv_len_hint),
-                                              _DTYPE_CODE[dtype])
+                                              _DTYPE_CODE[dtype], ctypes.byref(cs))
     _check("decode_attn_splits_for", s if s < 0 else 0)
-    return s
+    return s, cs.value
 
 
 def set_timing_events(before: "torch.cuda.Event | None", after: "torch.cuda.Event | None") -> None:

@@ -57,13 +57,14 @@ int check_sizes(int B, int n_head, int n_kv_head, int head_dim, int capacity, in
   return DA_OK;
 }
 
-size_t workspace_bytes_for(int B, int n_head, int splits, int head_dim) {
-  if (splits <= 1) return 0;
-  const size_t rows = (size_t)B * n_head * splits;
-  return rows * head_dim * sizeof(float) + rows * 2 * sizeof(float);
-}
-
 }  // namespace
+
+size_t workspace_bytes_for(int B, int n_head, int splits, int cluster, int head_dim) {
+  const int clusters = splits / (cluster > 0 ? cluster : 1);
+  if (clusters <= 1) return 0;
+  const size_t rows = (size_t)B * n_head * clusters;
+  return kCounterBytes + rows * (head_dim + 2) * sizeof(float);
+}
 
 bool decode_supported(int head_dim, int group) {
   return (head_dim == 64 || head_dim == 128) && (group == 1 || group == 2 || group == 4 || group == 8);
@@ -112,16 +113,28 @@ cudaError_t record_event(cudaEvent_t ev, cudaStream_t st) {
   return cudaEventRecord(ev, st);
 }
 
-// Splits for the current device: plan + occupancy of the instance.
-int plan_for_device(int dtype, int B, int n_kv_head, int head_dim, int group, int bound, int* splits) {
+// Splits and cluster size for the current device: plan + occupancy of the instance.
+int plan_for_device(int dtype, int B, int n_kv_head, int head_dim, int group, int bound, int* splits,
+                    int* cluster) {
   int device = 0, sms = 0;
   if (current_device(&device) != cudaSuccess) return DA_ERR_CUDA;
   if (device_sms(device, &sms) != cudaSuccess) return DA_ERR_CUDA;
   DecodeKernelInfo info;
   if (decode_kernel_info(dtype, head_dim, group, device, &info) != cudaSuccess) return DA_ERR_CUDA;
-  const int s = decode_attn_plan_splits(B, n_kv_head, head_dim, bound, sms, info.ctas_per_sm);
+  // the largest cluster size of which one cluster per group is co-resident
+  const int64_t units = (int64_t)B * n_kv_head;
+  int fit = 1;
+  for (int c = std::min(info.cluster_max, kMaxClusterSize); c >= 2; --c) {
+    if (info.active_clusters[c] >= units) {
+      fit = c;
+      break;
+    }
+  }
+  int cs = 1;
+  const int s = decode_attn_plan_splits(B, n_kv_head, head_dim, bound, sms, info.ctas_per_sm, fit, &cs);
   if (s < 1) return s;
   *splits = s;
+  *cluster = cs;
   return DA_OK;
 }
 
@@ -139,10 +152,10 @@ int decode_common(const void* q, const void* k_cache, const void* v_cache, void*
     return DA_ERR_ALIGN;
   const int group = n_head / n_kv_head;
   const int bound = max_kv_len_hint > 0 ? std::min(max_kv_len_hint, capacity) : capacity;
-  int splits = 1;
-  rc = plan_for_device(dtype, B, n_kv_head, head_dim, group, bound, &splits);
+  int splits = 1, cluster = 1;
+  rc = plan_for_device(dtype, B, n_kv_head, head_dim, group, bound, &splits, &cluster);
   if (rc != DA_OK) return rc;
-  const size_t need = workspace_bytes_for(B, n_head, splits, head_dim);
+  const size_t need = workspace_bytes_for(B, n_head, splits, cluster, head_dim);
   if (need > 0) {
     if (!workspace || workspace_bytes < need) return DA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return DA_ERR_ALIGN;
@@ -163,19 +176,22 @@ int decode_common(const void* q, const void* k_cache, const void* v_cache, void*
   p.n_kv_head = n_kv_head;
   p.capacity = capacity;
   p.splits = splits;
+  p.cluster = cluster;
+  p.len_hint = bound;
   p.qscale = scale * kLog2e;
   p.out = static_cast<uint8_t*>(out);
-  p.ws_acc = static_cast<float*>(workspace);
-  p.ws_ml = need > 0 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                                (size_t)B * n_head * splits * head_dim * sizeof(float))
-                     : nullptr;
+  if (need > 0) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.counters = reinterpret_cast<unsigned int*>(ws);
+    p.ws_acc = reinterpret_cast<float*>(ws + kCounterBytes);
+    p.ws_ml = p.ws_acc + (size_t)B * n_head * (splits / cluster) * head_dim;
+  }
   p.err_flag = err_flag;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (t_event_before && record_event(t_event_before, st) != cudaSuccess) return DA_ERR_CUDA;
   if (launch_decode(p, dtype, head_dim, group, st) != cudaSuccess) return DA_ERR_CUDA;
   if (t_event_after && record_event(t_event_after, st) != cudaSuccess) return DA_ERR_CUDA;
-  if (splits > 1 && launch_combine(p, dtype, head_dim, st) != cudaSuccess) return DA_ERR_CUDA;
   return DA_OK;
 }
 
@@ -200,17 +216,33 @@ const char* da_status_string(int status) {
 
 int da_version(void) { return 100; }
 
-int decode_attn_plan_splits(int B, int n_kv_head, int head_dim, int max_kv_len, int num_sms, int ctas_per_sm) {
-  if (B < 1 || n_kv_head < 1 || max_kv_len < 1 || num_sms < 1 || ctas_per_sm < 1) return DA_ERR_SHAPE;
+int decode_attn_plan_splits(int B, int n_kv_head, int head_dim, int max_kv_len, int num_sms, int ctas_per_sm,
+                            int cluster_max, int* cluster_size) {
+  if (B < 1 || n_kv_head < 1 || max_kv_len < 1 || num_sms < 1 || ctas_per_sm < 1 || cluster_max < 1)
+    return DA_ERR_SHAPE;
   if (head_dim != 64 && head_dim != 128) return DA_ERR_UNSUPPORTED;
   const int64_t units = (int64_t)B * n_kv_head;
-  const int64_t target = (int64_t)num_sms * ctas_per_sm;
-  int64_t s = (target + units - 1) / units;
+  const int64_t slots = (int64_t)num_sms * ctas_per_sm;  // CTAs resident at once
   const int rows = da::tile_rows(head_dim);
   const int64_t tiles = ((int64_t)max_kv_len + rows - 1) / rows;
-  s = std::min<int64_t>(s, tiles);
-  s = std::min<int64_t>(s, da::kMaxSplits);
-  return (int)std::max<int64_t>(s, 1);
+  // splits that fit one wave, at most one per tile
+  int64_t want = std::min<int64_t>({slots / units, tiles, (int64_t)da::kMaxSplits});
+  if (units > da::kMaxCounterGroups) want = 1;
+  int64_t cs = 1;
+  if (want >= 2) {
+    // Short prefixes are latency-bound: one cluster per group merges its
+    // splits on chip. Long ones are bandwidth-bound: spread the rows over
+    // every resident CTA and merge through the workspace.
+    const int64_t c = std::min<int64_t>({(int64_t)cluster_max, (int64_t)da::kMaxClusterSize, want});
+    if (c >= 2 && tiles <= da::kClusterTilesPerSplit * c) {
+      cs = c;
+      want = c;
+    }
+  } else {
+    want = 1;
+  }
+  if (cluster_size) *cluster_size = (int)cs;
+  return (int)want;
 }
 
 size_t decode_attn_workspace_size(int B, int n_head, int n_kv_head, int head_dim, int capacity) {
@@ -218,23 +250,34 @@ size_t decode_attn_workspace_size(int B, int n_head, int n_kv_head, int head_dim
   if (B == 0) return 0;
   size_t most = 0;
   for (int dtype = DA_F16; dtype <= DA_BF16; ++dtype) {
-    int splits = 1;
-    if (da::plan_for_device(dtype, B, n_kv_head, head_dim, n_head / n_kv_head, capacity, &splits) != DA_OK)
+    int splits = 1, cluster = 1;
+    if (da::plan_for_device(dtype, B, n_kv_head, head_dim, n_head / n_kv_head, capacity, &splits, &cluster) !=
+        DA_OK)
       return (size_t)-1;
-    most = std::max(most, da::workspace_bytes_for(B, n_head, splits, head_dim));
+    most = std::max(most, da::workspace_bytes_for(B, n_head, splits, cluster, head_dim));
   }
   return most;
 }
 
+int decode_attn_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace) return workspace_bytes == 0 ? DA_OK : DA_ERR_NULL;
+  if (cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return DA_ERR_CUDA;
+  return DA_OK;
+}
+
 int decode_attn_splits_for(int B, int n_head, int n_kv_head, int head_dim, int capacity, int max_kv_len_hint,
-                           int dtype) {
+                           int dtype, int* cluster_size) {
   int rc = da::check_sizes(B, n_head, n_kv_head, head_dim, capacity, dtype);
   if (rc != DA_OK) return rc;
-  if (B == 0) return 1;
-  const int bound = max_kv_len_hint > 0 ? std::min(max_kv_len_hint, capacity) : capacity;
-  int splits = 1;
-  rc = da::plan_for_device(dtype, B, n_kv_head, head_dim, n_head / n_kv_head, bound, &splits);
-  return rc != DA_OK ? rc : splits;
+  int splits = 1, cluster = 1;
+  if (B > 0) {
+    const int bound = max_kv_len_hint > 0 ? std::min(max_kv_len_hint, capacity) : capacity;
+    rc = da::plan_for_device(dtype, B, n_kv_head, head_dim, n_head / n_kv_head, bound, &splits, &cluster);
+    if (rc != DA_OK) return rc;
+  }
+  if (cluster_size) *cluster_size = cluster;
+  return splits;
 }
 
 int da_set_timing_events(void* event_before, void* event_after) {

@@ -16,19 +16,27 @@ namespace da {
 constexpr int32_t kErrKvLen = 1;
 constexpr int32_t kErrPosition = 2;
 constexpr int32_t kErrTimeout = 4;
+constexpr int32_t kErrWorkspace = 8;
 
 // A pipeline wait gives up after this long and reports kErrTimeout.
 constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
 
-// Decode kernel geometry. One stage holds kTileBytes of K rows and as many
-// bytes of V rows; kConsumerWarps warps compute, one more warp issues the
-// bulk copies.
-constexpr int kTileBytes = 8192;
-constexpr int kStages = 4;
-constexpr int kConsumerWarps = 4;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kDecodeThreads = kConsumerThreads + 32;
+// Decode kernel pipeline: one stage holds kTileBytes of K rows and as many
+// bytes of V rows.
+constexpr int kTileBytes = 16384;
 constexpr int kMaxSplits = 128;
+// Largest thread-block cluster of split CTAs (the non-portable hardware limit).
+constexpr int kMaxClusterSize = 16;
+// A group whose splits would stream at most this many tiles each is served
+// by one thread-block cluster (on-chip merge); longer prefixes are split
+// over every resident CTA and merged through the workspace.
+constexpr int kClusterTilesPerSplit = 4;
+// The workspace starts with one 32-bit arrival counter per (sequence, KV
+// head) group, in a fixed region so that calls of any shape find their
+// counters at the same place; split decoding is used only for at most
+// kMaxCounterGroups groups (more groups fill the GPU without splitting).
+constexpr int kMaxCounterGroups = 1024;
+constexpr int kCounterBytes = kMaxCounterGroups * 4;
 
 __host__ __device__ constexpr int tile_rows(int head_dim) { return kTileBytes / (2 * head_dim); }
 
@@ -112,6 +120,32 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, 
       : "memory");
 }
 
+// Bulk prefetch of global memory into L2 (no completion tracking). Address
+// 16-byte aligned, bytes a positive multiple of 16.
+__device__ __forceinline__ void prefetch_l2(const void* gmem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem), "r"(bytes) : "memory");
+}
+
+// Thread-block cluster barrier (every thread of every CTA of the cluster
+// arrives once per phase; release/acquire order the shared-memory writes
+// before it against the distributed reads after it).
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Load the float at the same shared-memory offset as `local` from the CTA of
+// the given rank in this cluster (distributed shared memory).
+__device__ __forceinline__ float ld_cluster_f32(const float* local, int rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
 // Programmatic dependent launch: wait for the preceding grid's memory, and
 // allow the following grid to be scheduled.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -147,6 +181,17 @@ struct Storage;
 
 template <>
 struct Storage<__nv_bfloat16> {
+  // a0 += q.lo * k.lo, a1 += q.hi * k.hi for two packed bf16 pairs, each
+  // product exact in fp32 and the sum rounded once (mixed-precision FMA).
+  static __device__ __forceinline__ void dot2(uint32_t q2, uint32_t k2, float& a0, float& a1) {
+    asm("{\n\t.reg .b16 ql, qh, kl, kh;\n\t"
+        "mov.b32 {ql, qh}, %2;\n\t"
+        "mov.b32 {kl, kh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, ql, kl, %0;\n\t"
+        "fma.rn.f32.bf16 %1, qh, kh, %1;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "r"(q2), "r"(k2));
+  }
   // 8 packed bf16 -> fp32 (exact: bf16 is the top half of an fp32).
   static __device__ __forceinline__ void unpack(const uint4& v, float (&f)[8]) {
     f[0] = __uint_as_float(v.x << 16);
@@ -158,12 +203,28 @@ struct Storage<__nv_bfloat16> {
     f[6] = __uint_as_float(v.w << 16);
     f[7] = __uint_as_float(v.w & 0xffff0000u);
   }
+  // 8 packed bf16 -> 4 fp32 pairs.
+  static __device__ __forceinline__ void unpack2(const uint4& v, float2 (&f)[4]) {
+    f[0] = make_float2(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u));
+    f[1] = make_float2(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+    f[2] = make_float2(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u));
+    f[3] = make_float2(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
+  }
   static __device__ __forceinline__ uint16_t round(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
   static constexpr uint16_t kNaN = 0x7FC0;
 };
 
 template <>
 struct Storage<__half> {
+  static __device__ __forceinline__ void dot2(uint32_t q2, uint32_t k2, float& a0, float& a1) {
+    asm("{\n\t.reg .b16 ql, qh, kl, kh;\n\t"
+        "mov.b32 {ql, qh}, %2;\n\t"
+        "mov.b32 {kl, kh}, %3;\n\t"
+        "fma.rn.f32.f16 %0, ql, kl, %0;\n\t"
+        "fma.rn.f32.f16 %1, qh, kh, %1;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "r"(q2), "r"(k2));
+  }
   static __device__ __forceinline__ float2 pair(uint32_t u) {
     __half2 h = *reinterpret_cast<__half2*>(&u);
     return __half22float2(h);
@@ -172,6 +233,12 @@ struct Storage<__half> {
     float2 a = pair(v.x), b = pair(v.y), c = pair(v.z), d = pair(v.w);
     f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
     f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+  }
+  static __device__ __forceinline__ void unpack2(const uint4& v, float2 (&f)[4]) {
+    f[0] = pair(v.x);
+    f[1] = pair(v.y);
+    f[2] = pair(v.z);
+    f[3] = pair(v.w);
   }
   static __device__ __forceinline__ uint16_t round(float x) { return __half_as_ushort(__float2half_rn(x)); }
   static constexpr uint16_t kNaN = 0x7E00;
@@ -189,10 +256,13 @@ struct DecodeParams {
   const int32_t* lens;     // kv_len, or position_ids when lens_are_positions
   int lens_are_positions;
   int B, n_head, n_kv_head, capacity, splits;
+  int len_hint;            // host bound on the active lengths (<= capacity), for L2 prefetch only
+  int cluster;             // CTAs per thread-block cluster along the split axis (divides splits)
   float qscale;            // softmax scale * log2(e)
   uint8_t* out;            // [B, n_head, D]
-  float* ws_acc;           // [B, n_head, splits, D]
-  float* ws_ml;            // [B, n_head, splits, 2]: running max (log2 units), sum
+  float* ws_acc;           // [B, n_head, splits / cluster, D]: one partial per cluster
+  float* ws_ml;            // [B, n_head, splits / cluster, 2]: running max (log2 units), sum
+  unsigned int* counters;  // [B, n_kv_head] arrival counters of the split groups
   int32_t* err_flag;       // may be null
 };
 

@@ -7,30 +7,77 @@
 
 namespace da {
 
+template <int D, int G>
+using ConfiguredShape = DecodeShape<D, G, DecodeConfig<D, G>::kWarps, DecodeConfig<D, G>::kPerLane,
+                                    DecodeConfig<D, G>::kStages>;
+
 template <typename T, int D, int G>
-cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream, const cudaLaunchAttribute* attr) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.splits, p.n_kv_head, p.B);
-  cfg.blockDim = dim3(kDecodeThreads);
-  cfg.dynamicSmemBytes = DecodeShape<D, G>::kSmemBytes;
-  cfg.stream = stream;
-  cfg.attrs = const_cast<cudaLaunchAttribute*>(attr);
-  cfg.numAttrs = attr ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, decode_split_kernel<T, D, G>, p);
+constexpr auto configured_kernel() {
+  return decode_split_kernel<T, D, G, DecodeConfig<D, G>::kWarps, DecodeConfig<D, G>::kPerLane,
+                             DecodeConfig<D, G>::kPackedK, DecodeConfig<D, G>::kStages>;
 }
 
-// Applies the shared-memory opt-in for the current device and reports the
-// occupancy of one instance.
+template <typename T, int D, int G>
+cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream, const cudaLaunchAttribute* pdl) {
+  using Shape = ConfiguredShape<D, G>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.splits, p.n_kv_head, p.B);
+  cfg.blockDim = dim3(Shape::kThreads);
+  cfg.dynamicSmemBytes = Shape::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attrs[2];
+  int n = 0;
+  if (pdl) attrs[n++] = *pdl;
+  if (p.cluster > 1) {
+    attrs[n].id = cudaLaunchAttributeClusterDimension;
+    attrs[n].val.clusterDim.x = p.cluster;
+    attrs[n].val.clusterDim.y = 1;
+    attrs[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, configured_kernel<T, D, G>(), p);
+}
+
+// Applies the shared-memory and cluster-size opt-ins for the current device
+// and reports the occupancy of one instance: resident CTAs per SM and the
+// largest cluster (16, else 8) of which at least one fits.
 template <typename T, int D, int G>
 cudaError_t decode_info_t(DecodeKernelInfo* info) {
-  const int smem = DecodeShape<D, G>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  using Shape = ConfiguredShape<D, G>;
+  const int smem = Shape::kSmemBytes;
+  auto* fn = configured_kernel<T, D, G>();
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   int n = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<T, D, G>, kDecodeThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, Shape::kThreads, smem);
   if (e != cudaSuccess) return e;
   info->smem_bytes = smem;
   info->ctas_per_sm = n;
+  info->cluster_max = 1;
+  for (int cs = 16; cs >= 1; --cs) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs, 1, 1);
+    cfg.blockDim = dim3(Shape::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = cs;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) != cudaSuccess) {
+      clusters = 0;
+      (void)cudaGetLastError();  // a refused size is not an error of the call
+    }
+    info->active_clusters[cs] = clusters;
+    if (clusters > 0 && info->cluster_max == 1) info->cluster_max = cs;
+  }
   return cudaSuccess;
 }
 

@@ -10,49 +10,355 @@
 //
 // Data path: one producer lane streams K and V tiles with bulk TMA copies
 // (cp.async.bulk, contiguous rows of the cache) into a kStages-deep ring of
-// shared-memory stages guarded by full/empty mbarriers. Four consumer warps
+// shared-memory stages guarded by full/empty mbarriers. CW consumer warps
 // read the stages with 128-bit shared loads: a row of D elements is spread
-// over D/8 lanes holding 8 elements each, and each lane keeps its slice of
-// the G query vectors in registers, pre-multiplied by scale * log2(e).
-// Scores are reduced across the lanes of a row with xor shuffles; every
-// group of lanes keeps an fp32 online-softmax state (running max m, sum l,
-// accumulator acc) in the base-2 domain (the max-subtracted fp32 softmax of
-// Cuda-Compute-OSS issue #343, "Proposed implementation"). At the end the
-// states of all lane groups and warps are merged; a sequence that needs a
-// single split writes `out` directly, otherwise the CTA writes its partial
-// (m, l, acc) for the combine kernel.
+// over D/DPL lanes holding DPL elements each (one or two 16-byte vectors),
+// and each lane keeps its slice of the G query vectors in registers,
+// pre-multiplied by scale * log2(e). Scores are reduced across the lanes of a
+// row with xor shuffles; every group of lanes keeps an fp32 online-softmax
+// state (running max m, sum l, accumulator acc) in the base-2 domain (the
+// max-subtracted fp32 softmax of Cuda-Compute-OSS issue #343, "Proposed
+// implementation").
+//
+// Merge of the splits. The splits of one (b, g) group are launched as
+// thread-block clusters of `cluster` CTAs. Each CTA folds its warps' states
+// into one (m, l, acc) in shared memory; after a cluster barrier every CTA
+// merges a slice of the G x D outputs over all CTAs of its cluster by reading
+// their states through distributed shared memory. A group served by one
+// cluster writes `out` there and then; a group served by several clusters
+// writes one partial per cluster to the workspace, and the last CTA to
+// arrive (a per-group counter) merges those partials into `out`.
 #pragma once
 
 #include "common.cuh"
 
 namespace da {
 
-template <int D, int G>
+// Largest cluster the merge supports (the hardware limit for non-portable
+// cluster sizes).
+constexpr int kMaxCluster = 16;
+
+template <int D, int G, int CW, int DPL, int NS>
 struct DecodeShape {
+  static constexpr int kStages = NS;                                 // depth of the shared-memory ring
+  static constexpr int kConsumerWarps = CW;
+  static constexpr int kConsumerThreads = CW * 32;
+  static constexpr int kThreads = kConsumerThreads + 32;             // + the producer warp
   static constexpr int kRowBytes = 2 * D;
-  static constexpr int kTileRows = kTileBytes / kRowBytes;          // 32 for D=128, 64 for D=64
-  static constexpr int kLanesPerRow = D / 8;                        // 16 or 8
-  static constexpr int kRowsPerStep = 32 / kLanesPerRow;            // rows a warp covers per step
-  static constexpr int kRowsPerWarp = kTileRows / kConsumerWarps;   // rows of a tile per warp
-  static constexpr int kSteps = kRowsPerWarp / kRowsPerStep;        // steps per tile per warp
-  static constexpr int kStageBytes = 2 * kTileBytes;                // K tile then V tile
+  static constexpr int kTileRows = kTileBytes / kRowBytes;           // 32 for D=128, 64 for D=64
+  static constexpr int kVecs = DPL / 8;                              // 16-byte vectors per lane per row
+  static constexpr int kLanesPerRow = D / DPL;
+  static constexpr int kRowsPerStep = 32 / kLanesPerRow;             // rows a warp covers per step
+  static constexpr int kRowsPerWarp = kTileRows / CW;                // rows of a tile per warp
+  static constexpr int kSteps = kRowsPerWarp / kRowsPerStep;         // steps per tile per warp
+  // When a quarter-warp (8 lanes, one shared-memory wavefront) spans two rows,
+  // odd rows visit their two vectors in the opposite order so that the eight
+  // 16-byte loads of a wavefront hit distinct banks.
+  static constexpr bool kSwap = kVecs == 2 && kLanesPerRow * 16 < 128;
+  static constexpr int kStageBytes = 2 * kTileBytes;                 // K tile then V tile
   static constexpr int kRingBytes = kStages * kStageBytes;
-  static constexpr int kReduceFloats = kConsumerWarps * G * (D + 2);
-  static constexpr int kSmemBytes = kRingBytes + kReduceFloats * 4 + 2 * kStages * 8 + 16;
-  static_assert(kRowsPerWarp % kRowsPerStep == 0, "tile rows must split evenly over warps");
+  static constexpr int kMergeFloats = CW * G * (D + 2);              // per-warp states
+  static constexpr int kStateFloats = G * D + 2 * G;                 // CTA state: acc[G][D], m[G], l[G]
+  static constexpr int kMlFloats = kMaxCluster * 2 * G;              // (m, l) gathered from the cluster
+  static constexpr int kSmemBytes = kRingBytes + kMergeFloats * 4 + 2 * kStages * 8 + 16;
+  static constexpr int kPerThread = (G * D + kConsumerThreads - 1) / kConsumerThreads;
+  static_assert(DPL == 8 || DPL == 16, "8 or 16 elements per lane");
+  static_assert(G <= kLanesPerRow, "the score reduction gives each head its own lanes");
+  static_assert(kRowsPerWarp % kRowsPerStep == 0 && kSteps >= 1, "tile rows must split evenly over warps");
+  static_assert(kStateFloats + kMlFloats <= kMergeFloats, "the CTA state reuses the per-warp merge area");
+  static_assert((kMergeFloats * 4) % 8 == 0, "mbarriers need 8-byte alignment");
 };
 
-template <typename T, int D, int G>
-__global__ void __launch_bounds__(kDecodeThreads) decode_split_kernel(const DecodeParams p) {
-  using Shape = DecodeShape<D, G>;
+// Consumer warps, elements per lane, score arithmetic and ring depth of each
+// instance. kPackedK: convert each K element once and form the G dot
+// products with packed fp32x2 FMAs on fp32 q (fewer instructions when
+// G >= 4); otherwise one mixed-precision FMA per element and head on the raw
+// 16-bit values. One CTA per SM with a 6-stage ring of 32 KiB stages (192 KiB)
+// keeps enough bytes in flight to cover the loaded HBM latency.
+template <int D, int G>
+struct DecodeConfig {
+  static constexpr int kWarps = G >= 4 ? 8 : 16;
+  static constexpr int kPerLane = G >= 4 ? 8 : 16;
+  static constexpr bool kPackedK = G == 4;
+  static constexpr int kStages = 6;
+};
+
+// Merge the per-warp (m, l, acc) states kept in shared memory for head g,
+// element d: returns the common max, the rescaled sum and accumulator.
+template <int D, int G, int CW>
+__device__ __forceinline__ void merge_warps(const float* red, int g, int d, float* mm_out, float* ls_out,
+                                            float* as_out) {
+  float mm = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < CW; ++w) mm = fmaxf(mm, red[(w * G + g) * (D + 2) + D]);
+  float ls = 0.f, as = 0.f;
+#pragma unroll
+  for (int w = 0; w < CW; ++w) {
+    const float* src = red + (w * G + g) * (D + 2);
+    const float mw = src[D];
+    const float f = (mw == -INFINITY) ? 0.f : fast_exp2(mw - mm);
+    ls = fmaf(src[D + 1], f, ls);
+    as = fmaf(src[d], f, as);
+  }
+  *mm_out = mm;
+  *ls_out = ls;
+  *as_out = as;
+}
+
+// Arrival counter of one (b, g) group: zero before the call, each CTA of the
+// group adds one, the arrival that completes the count is the last one and
+// puts the counter back to zero for the next call. Returns 1 for the last.
+// A count already at or past `arrivals` means the counter was not zero: that
+// is reported as kErrWorkspace and the CTA does not merge.
+__device__ __forceinline__ int arrive_count(unsigned int* counter, int arrivals, int32_t* err_flag) {
+  const unsigned int before = atomicAdd(counter, 1u);
+  if (before + 1u < (unsigned int)arrivals) return 0;
+  if (before + 1u > (unsigned int)arrivals) {
+    if (err_flag) atomicOr(err_flag, kErrWorkspace);
+    return 0;
+  }
+  atomicExch(counter, 0u);
+  return 1;
+}
+
+template <typename T>
+__device__ __forceinline__ void store_out(const DecodeParams& p, int64_t idx, float v) {
+  reinterpret_cast<uint16_t*>(p.out)[idx] = Storage<T>::round(v);
+}
+
+// A running max may lag the true max by up to 2^kLazyRescale (in base-2
+// units) before the accumulators are rescaled: the weights then stay below
+// 2^8, far from fp32 overflow, and rescales become rare.
+constexpr float kLazyRescale = 8.f;
+
+// One tile of K and V rows for one warp: scores of this lane group's rows
+// (mixed-precision FMAs on the raw 16-bit q and K, reduced over the lanes of
+// a row, then scaled), the lazily rescaled online-softmax update, and the
+// weighted V accumulation (packed fp32x2 FMAs). `kt`/`vt` point at this lane
+// group's first row of the tile; with kFull false only rows whose offset
+// from it is below `left` (in lane-group steps) are valid.
+template <typename S, typename Shape, int G, bool kFull, bool kPacked>
+__device__ __forceinline__ void consume_tile(const uint8_t* kt, const uint8_t* vt, int left,
+                                             const uint4 (&q)[G][Shape::kVecs],
+                                             const float2 (&qf)[kPacked ? G : 1][Shape::kVecs][4], float qscale,
+                                             int c, int swap, float (&m)[G], float& l_own,
+                                             float2 (&acc)[G][Shape::kVecs][4]) {
+  constexpr int NV = Shape::kVecs;
+  constexpr int LPR = Shape::kLanesPerRow;
+  constexpr int RS = Shape::kRowsPerStep * Shape::kRowBytes;  // bytes between a lane group's rows
+  float own[Shape::kSteps];  // this lane's head's score of each step's row
+#pragma unroll
+  for (int u = 0; u < Shape::kSteps; ++u) {
+    const bool valid = kFull || u * Shape::kRowsPerStep < left;
+    float part[G];
+    if constexpr (kPacked) {
+      float2 a[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) a[g] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < NV; ++j) {
+        uint4 kv = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) kv = *reinterpret_cast<const uint4*>(kt + u * RS + (c + LPR * (j ^ swap)) * 16);
+        float2 kf[4];
+        S::unpack2(kv, kf);
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) a[g] = __ffma2_rn(qf[g][j][e], kf[e], a[g]);
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) part[g] = a[g].x + a[g].y;
+    } else {
+      float a0[G], a1[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) a0[g] = a1[g] = 0.f;
+#pragma unroll
+      for (int j = 0; j < NV; ++j) {
+        uint4 kv = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) kv = *reinterpret_cast<const uint4*>(kt + u * RS + (c + LPR * (j ^ swap)) * 16);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          S::dot2(q[g][j].x, kv.x, a0[g], a1[g]);
+          S::dot2(q[g][j].y, kv.y, a0[g], a1[g]);
+          S::dot2(q[g][j].z, kv.z, a0[g], a1[g]);
+          S::dot2(q[g][j].w, kv.w, a0[g], a1[g]);
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) part[g] = a0[g] + a1[g];
+    }
+    // Sum over the LPR lanes of the row. With one head this is a butterfly.
+    // With several, each halving step sends the half of the heads this lane
+    // gives up and adds the partner's half of the ones it keeps; after
+    // log2(G) steps lane c holds head c / (LPR / G) alone, and the remaining
+    // steps add that one value.
+    if (G == 1) {
+      float v = part[0];
+#pragma unroll
+      for (int off = LPR / 2; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      own[u] = valid ? (kPacked ? v : v * qscale) : -INFINITY;
+    } else {
+#pragma unroll
+      for (int n = G, off = LPR / 2; n > 1; n >>= 1, off >>= 1) {
+        const bool upper = (c & off) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+          const float send = upper ? part[i] : part[i + n / 2];
+          const float keep = upper ? part[i + n / 2] : part[i];
+          part[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+      }
+      float v = part[0];
+#pragma unroll
+      for (int off = LPR / (2 * G); off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      own[u] = valid ? (kPacked ? v : v * qscale) : -INFINITY;
+    }
+  }
+
+  // Online softmax, one head per lane: the lane owns head `h` (all heads when
+  // G = 1), exponentiates only its head's scores and hands the weights to
+  // the other lanes of its row. The running max of every head is kept by
+  // every lane (the accumulators of all heads live in every lane); one vote
+  // per tile decides a (rare) lazy rescale of all heads.
+  const int h = G == 1 ? 0 : c / (LPR / G);
+  const int base = (threadIdx.x & 31) & ~(LPR - 1);
+  float mx = own[0];
+#pragma unroll
+  for (int u = 1; u < Shape::kSteps; ++u) mx = fmaxf(mx, own[u]);
+  float m_own = m[0];
+#pragma unroll
+  for (int g = 1; g < G; ++g) m_own = (h == g) ? m[g] : m_own;
+  if (__any_sync(0xffffffffu, mx > m_own + kLazyRescale)) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float mxg = G == 1 ? mx : __shfl_sync(0xffffffffu, mx, base + g * (LPR / G));
+      const float mnew = fmaxf(m[g], mxg);
+      const float alpha = (m[g] == -INFINITY) ? 0.f : fast_exp2(m[g] - mnew);
+      const float2 alpha2 = make_float2(alpha, alpha);
+#pragma unroll
+      for (int j = 0; j < NV; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[g][j][e] = __fmul2_rn(acc[g][j][e], alpha2);
+      if (g == h) l_own *= alpha;
+      m[g] = mnew;
+    }
+    m_own = m[0];
+#pragma unroll
+    for (int g = 1; g < G; ++g) m_own = (h == g) ? m[g] : m_own;
+  }
+  const bool none = (m_own == -INFINITY);  // no visible row yet for this head in this lane group
+  float pown[Shape::kSteps];
+#pragma unroll
+  for (int u = 0; u < Shape::kSteps; ++u) {
+    pown[u] = none ? 0.f : fast_exp2(own[u] - m_own);
+    l_own += pown[u];
+  }
+
+#pragma unroll
+  for (int u = 0; u < Shape::kSteps; ++u) {
+    const bool valid = kFull || u * Shape::kRowsPerStep < left;
+    float pb[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) pb[g] = G == 1 ? pown[u] : __shfl_sync(0xffffffffu, pown[u], base + g * (LPR / G));
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      uint4 vv = make_uint4(0u, 0u, 0u, 0u);
+      if (valid) vv = *reinterpret_cast<const uint4*>(vt + u * RS + (c + LPR * (j ^ swap)) * 16);
+      float2 vf[4];
+      S::unpack2(vv, vf);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float2 p2 = make_float2(pb[g], pb[g]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[g][j][e] = __ffma2_rn(p2, vf[e], acc[g][j][e]);
+      }
+    }
+  }
+}
+
+// Final merge of the per-cluster partials of one group by the last CTA to
+// arrive: out = sum_k 2^(m_k - M) acc_k / sum_k 2^(m_k - M) l_k over the P
+// clusters. The weights of every (head, cluster) are computed once into
+// shared memory (`buf`, at least G * (P + 1) floats); then each thread owns
+// one output per pass and a 1/R share of the clusters (R = threads per
+// output), with its loads independent so that they are all in flight.
+template <typename T, int D, int G, int NT>
+__device__ __forceinline__ void merge_partials(const DecodeParams& p, int64_t head0, int P, int nc, float* buf) {
+  constexpr int E = G * D;
+  float* wgt = buf;          // [G][P] weights
+  float* lsum = buf + G * P;  // [G]
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  for (int g = warp; g < G; g += NT / 32) {
+    const float* ml = p.ws_ml + (head0 + g) * nc * 2;
+    float mm = -INFINITY;
+    for (int k = lane; k < P; k += 32) mm = fmaxf(mm, __ldcg(ml + 2 * k));
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, off));
+    float ls = 0.f;
+    for (int k = lane; k < P; k += 32) {
+      const float mk = __ldcg(ml + 2 * k);
+      const float w = (mk == -INFINITY) ? 0.f : fast_exp2(mk - mm);
+      wgt[g * P + k] = w;
+      ls = fmaf(__ldcg(ml + 2 * k + 1), w, ls);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, off);
+    if (lane == 0) lsum[g] = ls;
+  }
+  __syncthreads();
+  constexpr int R = E >= NT ? 1 : NT / E;  // threads sharing one output
+  float* red = lsum + G;                   // [R][E] partial sums when R > 1
+  const int r = (int)threadIdx.x / E;      // this thread's share of the clusters (R > 1)
+  for (int i0 = 0; i0 < E; i0 += (R > 1 ? E : NT)) {
+    const int i = R > 1 ? (int)threadIdx.x % E : i0 + (int)threadIdx.x;
+    float as = 0.f;
+    if (i < E && r < R) {
+      const int g = i / D;
+      const float* part = p.ws_acc + (head0 + g) * nc * D + (i % D);
+      const float* w = wgt + g * P;
+      int k = R > 1 ? r : 0;
+      for (; k + 3 * R < P; k += 4 * R) {
+        const float v0 = __ldcg(part + (int64_t)k * D), v1 = __ldcg(part + (int64_t)(k + R) * D);
+        const float v2 = __ldcg(part + (int64_t)(k + 2 * R) * D), v3 = __ldcg(part + (int64_t)(k + 3 * R) * D);
+        as = fmaf(v0, w[k], as);
+        as = fmaf(v1, w[k + R], as);
+        as = fmaf(v2, w[k + 2 * R], as);
+        as = fmaf(v3, w[k + 3 * R], as);
+      }
+      for (; k < P; k += R) as = fmaf(__ldcg(part + (int64_t)k * D), w[k], as);
+    }
+    if (R > 1) {
+      if (r < R) red[r * E + i] = as;
+      __syncthreads();
+      if ((int)threadIdx.x < E) {
+        float t = 0.f;
+        for (int q = 0; q < R; ++q) t += red[q * E + threadIdx.x];
+        store_out<T>(p, head0 * D + threadIdx.x, t / lsum[threadIdx.x / D]);
+      }
+    } else if (i < E) {
+      store_out<T>(p, head0 * D + i, as / lsum[i / D]);
+    }
+  }
+}
+
+template <typename T, int D, int G, int CW, int DPL, bool PK, int NS>
+__global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const DecodeParams p) {
+  using Shape = DecodeShape<D, G, CW, DPL, NS>;
+  constexpr int kStages = NS;
   using S = Storage<T>;
   constexpr int LPR = Shape::kLanesPerRow;
+  constexpr int NV = Shape::kVecs;
+  constexpr int CT = Shape::kConsumerThreads;
+  constexpr int E = G * D;  // outputs of a group
 
   extern __shared__ __align__(128) uint8_t smem[];
   float* red = reinterpret_cast<float*>(smem + Shape::kRingBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Shape::kRingBytes + Shape::kReduceFloats * 4);
+  float* state = red;                          // acc[G][D], m[G], l[G] of this CTA, written over red
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + Shape::kMergeFloats);
   uint64_t* empty = full + kStages;
   int* abort_flag = reinterpret_cast<int*>(empty + kStages);
+  int* last_flag = abort_flag + 1;
 
   const int s = blockIdx.x;
   const int g_kv = blockIdx.y;
@@ -60,45 +366,79 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_split_kernel(const Deco
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int H = p.n_head;
+  const int CS = p.cluster;    // CTAs per cluster along the split axis
+  const int rank = s % CS;     // rank of this CTA in its cluster
+  const int cid = s / CS;      // which cluster of the group
+  const int64_t head0 = (int64_t)b * H + (int64_t)g_kv * G;
+  const int64_t kv_row0 = ((int64_t)b * p.n_kv_head + g_kv) * p.capacity;  // first cache row of this (b, g)
 
   pdl_trigger();
+  // Everything before pdl_wait() touches no memory the previous kernel on the
+  // stream may still write, except for L2 prefetches (L2 is coherent).
+  uint64_t policy = 0;
+  if (threadIdx.x == CT) {
+    policy = evict_first_policy();
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], CW);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    // Pull the first tiles this CTA will probably read into L2, with rows
+    // from the host's length bound (clamped to the cache).
+    const int lh = p.len_hint;
+    const int ch = split_chunk(lh, p.splits, Shape::kTileRows);
+    const int pr0 = s * ch;
+    if (pr0 < lh) {
+      const int rows = min(min(ch, lh - pr0), kStages * Shape::kTileRows);
+      const int64_t off = (kv_row0 + pr0) * Shape::kRowBytes;
+      prefetch_l2(p.k_cache + off, rows * Shape::kRowBytes);
+      prefetch_l2(p.v_cache + off, rows * Shape::kRowBytes);
+    }
+  }
+  __syncthreads();
   pdl_wait();
+
+  // Lane layout of the consumers: lane group `lrow` of a step takes one row;
+  // within it, lane c holds vectors c + LPR * j (j < NV) of the row, slot j
+  // visiting vector c + LPR * (j ^ swap).
+  const int c = lane % LPR;
+  const int lrow = lane / LPR;
+  const int swap = Shape::kSwap ? (lrow & 1) : 0;
+  uint4 qraw[G][NV];
+  if (warp < CW) {  // q loads overlap the length load below
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int j = 0; j < NV; ++j)
+        qraw[g][j] = ld_global_nc_v4(p.q + ((head0 + g) * D + (c + LPR * (j ^ swap)) * 8) * 2);
+  }
 
   int32_t err_bits = 0;
   const int L = sequence_length(p, b, &err_bits);
   if (L < 0) {
-    // Invalid input: split 0 writes NaN rows for the group's heads.
+    // Invalid input (the same for every CTA of the group, so whole clusters
+    // leave here): split 0 writes NaN rows for the group's heads.
     if (s == 0) {
-      for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-        const int64_t o = ((int64_t)b * H + (int64_t)g_kv * G) * D + i;
-        reinterpret_cast<uint16_t*>(p.out)[o] = S::kNaN;
-      }
+      for (int i = threadIdx.x; i < E; i += Shape::kThreads)
+        reinterpret_cast<uint16_t*>(p.out)[head0 * D + i] = S::kNaN;
       if (threadIdx.x == 0 && p.err_flag) atomicOr(p.err_flag, err_bits);
     }
     return;
   }
   const int chunk = split_chunk(L, p.splits, Shape::kTileRows);
   const int nsplit = active_splits(L, chunk);
-  if (s >= nsplit) return;
-  const int r0 = s * chunk;
+  const int nclusters = (nsplit + CS - 1) / CS;  // clusters with at least one active split
+  if (cid >= nclusters) return;                   // the whole cluster is idle
+  // Splits past nsplit in an active cluster read nothing and contribute an
+  // empty state (m = -inf, l = 0), but take part in the cluster barriers.
+  const int r0 = min(s * chunk, L);
   const int r1 = min(L, r0 + chunk);
   const int ntiles = (r1 - r0 + Shape::kTileRows - 1) / Shape::kTileRows;
   const bool fused = p.k_new != nullptr;
+  const int64_t new_row = ((int64_t)b * p.n_kv_head + g_kv) * D;  // element offset into k_new
 
-  const int64_t kv_row0 = ((int64_t)b * p.n_kv_head + g_kv) * p.capacity;  // first row of this (b, g)
-  const int64_t new_row = ((int64_t)b * p.n_kv_head + g_kv) * D;           // element offset into k_new
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kConsumerWarps);
-    }
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  if (warp == kConsumerWarps) {
+  if (warp == CW) {
     // ---------------- producer warp ----------------
     if (fused && s == 0 && lane < D / 8) {
       // The new row goes into the cache; no CTA of this launch reads it back
@@ -109,7 +449,6 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_split_kernel(const Deco
       *reinterpret_cast<uint4*>(p.v_cache_w + dst) = ld_global_nc_v4(p.v_new + src);
     }
     if (lane == 0) {
-      const uint64_t policy = evict_first_policy();
       int issued = 0;
       for (int t = 0; t < ntiles; ++t) {
         const int stage = t % kStages;
@@ -146,181 +485,215 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_split_kernel(const Deco
       }
     }
     __syncwarp();
-    return;  // the producer warp takes no part in the epilogue
-  }
-
-  // ---------------- consumer warps ----------------
-  const int c = lane % LPR;     // which 8-element slice of a row
-  const int lrow = lane / LPR;  // which row of a step
-
-  float qf[G][8];
+  } else {
+    // ---------------- consumer warps ----------------
+    float m[G], l_own = 0.f;  // running max of every head; weight sum of this lane's head
+    float2 acc[G][NV][4];
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const int64_t qoff = (((int64_t)b * H + (int64_t)g_kv * G + g) * D + c * 8) * 2;
-    float f[8];
-    S::unpack(ld_global_nc_v4(p.q + qoff), f);
+    for (int g = 0; g < G; ++g) {
+      m[g] = -INFINITY;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) qf[g][e] = f[e] * p.qscale;
-  }
-
-  float m[G], l[G], acc[G][8];
+      for (int j = 0; j < NV; ++j)
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    m[g] = -INFINITY;
-    l[g] = 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
-  }
-
-  bool aborted = false;
-  for (int t = 0; t < ntiles; ++t) {
-    const int stage = t % kStages;
-    const bool ok_wait = mbar_wait(&full[stage], (t / kStages) & 1);
-    if (__any_sync(0xffffffffu, !ok_wait)) {
-      aborted = true;
-      break;
+        for (int e = 0; e < 4; ++e) acc[g][j][e] = make_float2(0.f, 0.f);
     }
-    const uint8_t* kt = smem + stage * Shape::kStageBytes;
-    const uint8_t* vt = kt + kTileBytes;
-    const int rows = min(Shape::kTileRows, r1 - (r0 + t * Shape::kTileRows));
-
-    float sc[Shape::kSteps][G];
+    const int lane_off = (warp * Shape::kRowsPerWarp + lrow) * Shape::kRowBytes;
+    float2 qf[PK ? G : 1][NV][4];  // fp32 q pre-multiplied by the scale (packed path only)
+    if constexpr (PK) {
 #pragma unroll
-    for (int u = 0; u < Shape::kSteps; ++u) {
-      const int r = warp * Shape::kRowsPerWarp + u * Shape::kRowsPerStep + lrow;
-      const bool valid = r < rows;
-      uint4 kv = make_uint4(0u, 0u, 0u, 0u);
-      if (valid) kv = ld_shared_v4(kt + r * Shape::kRowBytes + c * 16);
-      float kf[8];
-      S::unpack(kv, kf);
-      float part[G];
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+          float2 f[4];
+          S::unpack2(qraw[g][j], f);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) qf[g][j][e] = make_float2(f[e].x * p.qscale, f[e].y * p.qscale);
+        }
+    }
+
+    bool aborted = false;
+    for (int t = 0; t < ntiles; ++t) {
+      const int stage = t % kStages;
+      const bool ok_wait = mbar_wait(&full[stage], (t / kStages) & 1);
+      if (__any_sync(0xffffffffu, !ok_wait)) {
+        aborted = true;
+        break;
+      }
+      const uint8_t* kt = smem + stage * Shape::kStageBytes + lane_off;
+      const uint8_t* vt = kt + kTileBytes;
+      const int rows = min(Shape::kTileRows, r1 - (r0 + t * Shape::kTileRows));
+      if (rows == Shape::kTileRows) {
+        consume_tile<S, Shape, G, true, PK>(kt, vt, 0, qraw, qf, p.qscale, c, swap, m, l_own, acc);
+      } else {
+        consume_tile<S, Shape, G, false, PK>(kt, vt, rows - (warp * Shape::kRowsPerWarp + lrow), qraw, qf,
+                                             p.qscale, c, swap, m, l_own, acc);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+    }
+    if (aborted) atomicOr(abort_flag, 1);
+
+    // Back to the canonical slot order (slot j = vector c + LPR * j).
+    if (Shape::kSwap) {
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 a0 = acc[g][0][e], a1 = acc[g][NV - 1][e];
+          acc[g][0][e] = swap ? a1 : a0;
+          acc[g][NV - 1][e] = swap ? a0 : a1;
+        }
+    }
+
+    // Weight sums of all heads (each lane kept its own head's).
+    float l[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      l[g] = G == 1 ? l_own : __shfl_sync(0xffffffffu, l_own, (lane & ~(LPR - 1)) + g * (LPR / G));
+
+    // Merge the lane groups of the warp that hold the same vectors.
+#pragma unroll
+    for (int off = LPR; off < 32; off <<= 1) {
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        float a0 = qf[g][0] * kf[0];
-        float a1 = qf[g][1] * kf[1];
-        a0 = fmaf(qf[g][2], kf[2], a0);
-        a1 = fmaf(qf[g][3], kf[3], a1);
-        a0 = fmaf(qf[g][4], kf[4], a0);
-        a1 = fmaf(qf[g][5], kf[5], a1);
-        a0 = fmaf(qf[g][6], kf[6], a0);
-        a1 = fmaf(qf[g][7], kf[7], a1);
-        part[g] = a0 + a1;
+        const float mo = __shfl_xor_sync(0xffffffffu, m[g], off);
+        const float lo = __shfl_xor_sync(0xffffffffu, l[g], off);
+        const float mm = fmaxf(m[g], mo);
+        const float fa = (m[g] == -INFINITY) ? 0.f : fast_exp2(m[g] - mm);
+        const float fb = (mo == -INFINITY) ? 0.f : fast_exp2(mo - mm);
+        l[g] = l[g] * fa + lo * fb;
+#pragma unroll
+        for (int j = 0; j < NV; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float ax = __shfl_xor_sync(0xffffffffu, acc[g][j][e].x, off);
+            const float ay = __shfl_xor_sync(0xffffffffu, acc[g][j][e].y, off);
+            acc[g][j][e] = make_float2(acc[g][j][e].x * fa + ax * fb, acc[g][j][e].y * fa + ay * fb);
+          }
+        m[g] = mm;
       }
-#pragma unroll
-      for (int off = LPR / 2; off >= 1; off >>= 1) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) part[g] += __shfl_xor_sync(0xffffffffu, part[g], off);
-      }
-#pragma unroll
-      for (int g = 0; g < G; ++g) sc[u][g] = valid ? part[g] : -INFINITY;
     }
 
-    float pw[Shape::kSteps][G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float mx = sc[0][g];
-#pragma unroll
-      for (int u = 1; u < Shape::kSteps; ++u) mx = fmaxf(mx, sc[u][g]);
-      const float mnew = fmaxf(m[g], mx);
-      const bool none = (mnew == -INFINITY);  // no visible row yet in this lane group
-      const float alpha = none ? 1.f : fast_exp2(m[g] - mnew);
-      float add = 0.f;
-#pragma unroll
-      for (int u = 0; u < Shape::kSteps; ++u) {
-        pw[u][g] = none ? 0.f : fast_exp2(sc[u][g] - mnew);
-        add += pw[u][g];
-      }
-      l[g] = fmaf(l[g], alpha, add);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[g][e] *= alpha;
-      m[g] = mnew;
-    }
-
-#pragma unroll
-    for (int u = 0; u < Shape::kSteps; ++u) {
-      const int r = warp * Shape::kRowsPerWarp + u * Shape::kRowsPerStep + lrow;
-      uint4 vv = make_uint4(0u, 0u, 0u, 0u);
-      if (r < rows) vv = ld_shared_v4(vt + r * Shape::kRowBytes + c * 16);
-      float vf[8];
-      S::unpack(vv, vf);
+    // Per-warp states to shared memory: red[warp][g][0..D) = acc, [D] = m, [D+1] = l.
+    if (lrow == 0) {
 #pragma unroll
       for (int g = 0; g < G; ++g) {
+        float* dst = red + (warp * G + g) * (D + 2);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[g][e] = fmaf(pw[u][g], vf[e], acc[g][e]);
+        for (int j = 0; j < NV; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            dst[(c + LPR * j) * 8 + 2 * e] = acc[g][j][e].x;
+            dst[(c + LPR * j) * 8 + 2 * e + 1] = acc[g][j][e].y;
+          }
+        if (c == 0) {
+          dst[D] = m[g];
+          dst[D + 1] = l[g];
+        }
       }
     }
+    asm volatile("bar.sync 1, %0;" ::"n"(CT) : "memory");
 
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[stage]);
-  }
-  if (aborted) atomicOr(abort_flag, 1);
-
-  // Merge the lane groups of the warp that hold the same slice c.
+    // Fold the warps into this CTA's state. A CTA whose pipeline timed out
+    // publishes NaN, which poisons every output of its group.
+    const bool failed = *reinterpret_cast<volatile int*>(abort_flag) != 0;
+    if (failed && threadIdx.x == 0 && p.err_flag) atomicOr(p.err_flag, kErrTimeout);
+    float va[Shape::kPerThread], vm[Shape::kPerThread], vl[Shape::kPerThread];
 #pragma unroll
-  for (int off = LPR; off < 32; off <<= 1) {
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float mo = __shfl_xor_sync(0xffffffffu, m[g], off);
-      const float lo = __shfl_xor_sync(0xffffffffu, l[g], off);
-      const float mm = fmaxf(m[g], mo);
-      const float fa = (m[g] == -INFINITY) ? 0.f : fast_exp2(m[g] - mm);
-      const float fb = (mo == -INFINITY) ? 0.f : fast_exp2(mo - mm);
-      l[g] = l[g] * fa + lo * fb;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float ao = __shfl_xor_sync(0xffffffffu, acc[g][e], off);
-        acc[g][e] = acc[g][e] * fa + ao * fb;
-      }
-      m[g] = mm;
+    for (int k = 0; k < Shape::kPerThread; ++k) {
+      const int i = threadIdx.x + k * CT;
+      if (i < E) merge_warps<D, G, CW>(red, i / D, i % D, &vm[k], &vl[k], &va[k]);
     }
-  }
-
-  // Per-warp states to shared memory: red[warp][g][0..D) = acc, [D] = m, [D+1] = l.
-  if (lrow == 0) {
+    asm volatile("bar.sync 1, %0;" ::"n"(CT) : "memory");  // red is read; state overwrites it
+    const float nan = __int_as_float(0x7fc00000);
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float* dst = red + (warp * G + g) * (D + 2);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) dst[c * 8 + e] = acc[g][e];
-      if (c == 0) {
-        dst[D] = m[g];
-        dst[D + 1] = l[g];
+    for (int k = 0; k < Shape::kPerThread; ++k) {
+      const int i = threadIdx.x + k * CT;
+      if (i < E) {
+        state[i] = failed ? nan : va[k];
+        if (i % D == 0) {
+          state[E + i / D] = failed ? nan : vm[k];
+          state[E + G + i / D] = vl[k];
+        }
       }
     }
   }
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+  __syncthreads();
 
-  const bool failed = *reinterpret_cast<volatile int*>(abort_flag) != 0;
-  if (failed && threadIdx.x == 0 && p.err_flag) atomicOr(p.err_flag, kErrTimeout);
-
-  for (int i = threadIdx.x; i < G * D; i += kConsumerThreads) {
+  // ---------------- merge over the cluster ----------------
+  // Each CTA merges a slice of the E outputs over the CS CTAs of its
+  // cluster, reading their states through distributed shared memory: first
+  // the (m, l) of every head of every rank (one load per thread), then for
+  // each output the CS accumulators (independent loads, all in flight).
+  float* mlbuf = state + Shape::kStateFloats;  // [cluster][2G]
+  if (CS > 1) {
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    for (int t = threadIdx.x; t < CS * 2 * G; t += Shape::kThreads)
+      mlbuf[t] = ld_cluster_f32(state + E + t % (2 * G), t / (2 * G));
+    __syncthreads();
+  }
+  const int per = (E + CS - 1) / CS;  // outputs merged by each CTA of the cluster
+  const int e0 = rank * per;
+  const int e1 = min(E, e0 + per);
+  for (int i = e0 + (int)threadIdx.x; i < e1; i += Shape::kThreads) {
     const int g = i / D;
     const int d = i % D;
-    float mm = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) mm = fmaxf(mm, red[(w * G + g) * (D + 2) + D]);
-    float ls = 0.f, as = 0.f;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
-      const float* src = red + (w * G + g) * (D + 2);
-      const float mw = src[D];
-      const float f = (mw == -INFINITY) ? 0.f : fast_exp2(mw - mm);
-      ls = fmaf(src[D + 1], f, ls);
-      as = fmaf(src[d], f, as);
-    }
-    const int h = g_kv * G + g;
-    if (nsplit == 1) {
-      const int64_t o = ((int64_t)b * H + h) * D + d;
-      reinterpret_cast<uint16_t*>(p.out)[o] = failed ? S::kNaN : S::round(as / ls);
+    float mm, ls, as;
+    if (CS == 1) {
+      mm = state[E + g];
+      ls = state[E + G + g];
+      as = state[i];
     } else {
-      const int64_t base = ((int64_t)b * H + h) * p.splits + s;
-      p.ws_acc[base * D + d] = failed ? __int_as_float(0x7fc00000) : as;
+      float a[kMaxCluster];
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r) a[r] = r < CS ? ld_cluster_f32(state + i, r) : 0.f;
+      mm = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r)
+        if (r < CS) mm = fmaxf(mm, mlbuf[r * 2 * G + g]);
+      ls = 0.f;
+      as = 0.f;
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r) {
+        if (r < CS) {
+          const float mr = mlbuf[r * 2 * G + g];
+          const float f = (mr == -INFINITY) ? 0.f : fast_exp2(mr - mm);
+          ls = fmaf(mlbuf[r * 2 * G + G + g], f, ls);
+          as = fmaf(a[r], f, as);
+        }
+      }
+    }
+    if (nclusters == 1) {
+      store_out<T>(p, head0 * D + i, as / ls);
+    } else {
+      const int64_t base = (head0 + g) * (p.splits / CS) + cid;
+      p.ws_acc[base * D + d] = as;
       if (d == 0) {
-        p.ws_ml[base * 2] = failed ? __int_as_float(0x7fc00000) : mm;
+        p.ws_ml[base * 2] = mm;
         p.ws_ml[base * 2 + 1] = ls;
       }
     }
   }
+  if (CS > 1) cluster_arrive_release();  // this CTA is done reading the others' states
+
+  if (nclusters > 1) {
+    // Several clusters: the last CTA of the group to arrive merges the
+    // cluster partials (written by other SMs, so read from L2).
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const int last = arrive_count(p.counters + (int64_t)b * p.n_kv_head + g_kv, nclusters * CS, p.err_flag);
+      *reinterpret_cast<volatile int*>(last_flag) = last;
+    }
+    __syncthreads();
+    if (*reinterpret_cast<volatile int*>(last_flag)) {
+      __threadfence();
+      // the ring is idle now; the cluster may still be reading `state`
+      merge_partials<T, D, G, Shape::kThreads>(p, head0, nclusters, p.splits / CS, reinterpret_cast<float*>(smem));
+    }
+  }
+  if (CS > 1) cluster_wait_acquire();  // keep this CTA's state alive until the cluster has read it
 }
 
 }  // namespace da

@@ -13,12 +13,18 @@ namespace da {
 struct DecodeKernelInfo {
   int smem_bytes;
   int ctas_per_sm;
+  int cluster_max;              // largest cluster size that can be resident
+  int active_clusters[17];      // clusters of each size (1..16) resident at once
 };
 
 bool decode_supported(int head_dim, int group);
 cudaError_t decode_kernel_info(int dtype, int head_dim, int group, int device, DecodeKernelInfo* info);
 cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int group, cudaStream_t stream);
-cudaError_t launch_combine(const DecodeParams& p, int dtype, int head_dim, cudaStream_t stream);
+// Scratch bytes of one decode call with `splits` splits in clusters of
+// `cluster`: none when one cluster serves a group; otherwise a fixed region
+// of 32-bit arrival counters, then fp32 per-cluster partials
+// acc [B, n_head, splits / cluster, D] and (m, l) [B, n_head, splits / cluster, 2].
+size_t workspace_bytes_for(int B, int n_head, int splits, int cluster, int head_dim);
 cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                           const int32_t* pos, int B, int n_kv_head, int head_dim, int capacity,
                           int32_t* err_flag, cudaStream_t stream);

@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "decode_attn.h"
+#include "launch.h"
 
 namespace {
 
@@ -20,14 +21,17 @@ void* g_scratch_ptr[kMaxDevices] = {};
 std::mutex g_scratch_mutex;
 
 // Device address of g_static_scratch on the current device, looked up once
-// per device with that device current. Returns DA_OK or DA_ERR_CUDA.
-int scratch_address(void** out) {
+// per device with that device current; the same set-up zero-fills the
+// arrival counters at the start of the array on `stream` (ahead of the
+// call's kernel). Returns DA_OK or DA_ERR_CUDA.
+int scratch_address(void** out, cudaStream_t stream) {
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices) return DA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
   if (!g_scratch_ptr[device]) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) return DA_ERR_CUDA;
+    if (cudaMemsetAsync(ptr, 0, da::kCounterBytes, stream) != cudaSuccess) return DA_ERR_CUDA;
     g_scratch_ptr[device] = ptr;
   }
   *out = g_scratch_ptr[device];
@@ -41,15 +45,17 @@ extern "C" int decode_attn_fwd_static_scratch(const void* q, const void* k_cache
                                               int head_dim, int capacity, float scale, void* out,
                                               int max_kv_len_hint, int dtype, int32_t* err_flag,
                                               void* stream) {
-  // The split count this call will use decides how much scratch it needs:
-  // fp32 partials [B, n_head, S, head_dim + 2] when S > 1, none when S = 1.
-  const int splits = decode_attn_splits_for(B, n_head, n_kv_head, head_dim, capacity, max_kv_len_hint, dtype);
+  // The split count this call will use decides how much scratch it needs
+  // (none when it is 1).
+  int cluster = 1;
+  const int splits =
+      decode_attn_splits_for(B, n_head, n_kv_head, head_dim, capacity, max_kv_len_hint, dtype, &cluster);
   if (splits < 0) return splits;
-  const size_t need = splits > 1 ? (size_t)B * n_head * splits * (head_dim + 2) * sizeof(float) : 0;
+  const size_t need = da::workspace_bytes_for(B, n_head, splits, cluster, head_dim);
   if (need > DA_STATIC_SCRATCH_BYTES) return DA_ERR_SHAPE;
   void* scratch = nullptr;
   if (need > 0) {
-    const int rc = scratch_address(&scratch);
+    const int rc = scratch_address(&scratch, static_cast<cudaStream_t>(stream));
     if (rc != DA_OK) return rc;
   }
   return decode_attn_fwd(q, k_cache, v_cache, kv_len, B, n_head, n_kv_head, head_dim, capacity, scale, out, scratch,

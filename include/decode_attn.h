@@ -73,6 +73,7 @@ typedef enum {
 #define DA_DEVERR_KV_LEN 1u   /* some kv_len[b] outside [1, capacity]: rows of b are NaN */
 #define DA_DEVERR_POSITION 2u /* some position_ids[b] outside [0, capacity): write skipped */
 #define DA_DEVERR_TIMEOUT 4u  /* a pipeline wait hit its time limit: rows are NaN */
+#define DA_DEVERR_WORKSPACE 8u /* the workspace counters were not zero: outputs not written */
 
 /* Human-readable name of a da_status value (static string). */
 DA_API const char* da_status_string(int status);
@@ -82,32 +83,51 @@ DA_API int da_version(void);
 
 /*
  * Split plan of the decode kernel, a pure host computation (no CUDA call):
- * the number of KV splits S per (sequence, KV head) for B sequences,
- * n_kv_head KV heads, head_dim, a bound on the active length max_kv_len, and
- * a GPU with num_sms multiprocessors running ctas_per_sm decode CTAs each.
- * Each sequence b then splits its own kv_len[b] rows evenly over at most S
- * CTAs, in whole tiles. Returns S >= 1, or a negative da_status.
+ * the number of KV splits S per (sequence, KV head) group for B sequences,
+ * n_kv_head KV heads, head_dim and a bound max_kv_len on the active length,
+ * on a GPU with num_sms multiprocessors holding ctas_per_sm decode CTAs each,
+ * where one thread-block cluster of up to cluster_max CTAs per group can be
+ * resident. S is as many splits as fit one wave of resident CTAs, at most
+ * one per tile of max_kv_len rows and at most 128. When each split would
+ * stream at most 4 tiles (a latency-bound short prefix) and cluster_max >= 2,
+ * the splits of a group form one cluster of *cluster_size = S CTAs that
+ * merge their partial softmax states through distributed shared memory;
+ * otherwise *cluster_size = 1 and the partials go through the workspace.
+ * (*cluster_size is written when non-NULL.) Each sequence b then splits its
+ * own kv_len[b] rows evenly over at most S CTAs, in whole tiles.
+ * Returns S >= 1, or a negative da_status.
  */
 DA_API int decode_attn_plan_splits(int B, int n_kv_head, int head_dim, int max_kv_len, int num_sms,
-                            int ctas_per_sm);
+                                   int ctas_per_sm, int cluster_max, int* cluster_size);
 
 /*
  * Bytes of scratch memory decode_attn_fwd / decode_step_fwd need for these
  * sizes on the current device, for any max_kv_len_hint <= capacity.
- * Returns 0 when no scratch is needed, or (size_t)-1 for invalid sizes or a
- * failed device query. The workspace holds fp32 partial results
- * [B, n_head, S, head_dim + 2]; it needs no initialisation.
+ * Returns 0 when no scratch is needed (one cluster serves each group), or
+ * (size_t)-1 for invalid sizes or a failed device query. Otherwise the
+ * workspace starts with a 4 KiB region of 32-bit arrival counters (one per
+ * sequence and KV head), followed by fp32 per-cluster partials
+ * [B, n_head, S / cluster, head_dim + 2]. It must be zero-filled once before
+ * its first use (decode_attn_workspace_init, or any memset); every call that
+ * completes leaves it ready for the next call of any shape. After a
+ * DA_DEVERR_TIMEOUT or DA_DEVERR_WORKSPACE, zero it again.
  */
 DA_API size_t decode_attn_workspace_size(int B, int n_head, int n_kv_head, int head_dim, int capacity);
 
+/* Zero-fill a workspace on `stream` (cudaMemsetAsync; allocates nothing). */
+DA_API int decode_attn_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * The split count S that decode_attn_fwd / decode_step_fwd will use for
- * these arguments on the current device (1 means a single launch that writes
- * out directly; S > 1 adds the combine launch and needs the workspace).
+ * these arguments on the current device, and (when cluster_size is non-NULL)
+ * the cluster size. S == 1: one CTA per group writes out directly; S equal
+ * to the cluster size: one cluster per group merges in distributed shared
+ * memory, no workspace; S larger: one partial per cluster goes through the
+ * workspace and the last CTA of each group merges them, in the same launch.
  * Returns S >= 1 or a negative da_status.
  */
 DA_API int decode_attn_splits_for(int B, int n_head, int n_kv_head, int head_dim, int capacity,
-                                  int max_kv_len_hint, int dtype);
+                                  int max_kv_len_hint, int dtype, int* cluster_size);
 
 /*
  * Profiling hook. When both are non-NULL, every later decode_attn_fwd /
@@ -179,18 +199,20 @@ DA_API int decode_step_fwd(const void* q, void* k_cache, void* v_cache, const vo
  * library holds on every GPU that loads it, until the process exits. Nothing
  * is allocated or freed by the call.
  *
- * - The first call on a device looks up that array's device address
- *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture on the device.
+ * - The first call on a device that needs scratch looks up that array's
+ *   device address (cudaGetSymbolAddress, with that device current) and
+ *   zero-fills its arrival counters on `stream`; make that first call before
+ *   any stream capture on the device.
  * - Arguments whose split plan needs more scratch than
  *   DA_STATIC_SCRATCH_BYTES (decode_attn_workspace_size-style need for this
  *   call's max_kv_len_hint) are rejected with DA_ERR_SHAPE before anything is
  *   enqueued; use decode_attn_fwd with your own workspace for those.
  * - Every call on a device shares the one array and leaves its partials in
- *   it. The kernels write every partial they later read, so nothing needs to
- *   start at zero, but calls that overlap on the GPU (different streams
- *   without ordering, or different host threads) race on the array and give
- *   wrong results: keep such calls ordered.
+ *   it. The kernels write every partial they later read, and every completed
+ *   call leaves the arrival counters at zero again, so nothing has to be
+ *   cleared between calls; but calls that overlap on the GPU (different
+ *   streams without ordering, or different host threads) race on the array
+ *   and give wrong results: keep such calls ordered.
  * Otherwise identical to decode_attn_fwd, including results bit for bit.
  */
 DA_API int decode_attn_fwd_static_scratch(const void* q, const void* k_cache, const void* v_cache,

@@ -54,25 +54,33 @@ def test_status_strings(lib):
 
 def test_plan_splits_properties(lib):
     sms, per = 152, 3
-    # one (b, kv-head) unit per CTA already fills the GPU: no split
-    assert da.plan_splits(64, 8, 128, 32768, sms, per) == 1
-    # long context, 8 units: enough splits for a full wave
-    s = da.plan_splits(1, 8, 128, 32768, sms, per)
-    assert s * 8 >= sms * per and s <= 128
-    # never more splits than 32-row tiles (D=128) or 64-row tiles (D=64)
-    assert da.plan_splits(1, 1, 128, 40, sms, per) == 2
-    assert da.plan_splits(1, 1, 64, 40, sms, per) == 1
-    assert da.plan_splits(1, 1, 128, 1, sms, per) == 1
-    # monotone in the length bound, so a workspace sized for capacity fits any hint
-    prev = 0
-    for n in range(1, 9000, 37):
-        cur = da.plan_splits(1, 16, 128, n, sms, per)
-        assert cur >= prev
-        prev = cur
-    for bad in [(0, 8, 128, 10, sms, per), (1, 0, 128, 10, sms, per), (1, 8, 128, 0, sms, per),
-                (1, 8, 128, 10, 0, per), (1, 8, 128, 10, sms, 0)]:
-        assert lib.decode_attn_plan_splits(*bad) == -2
-    assert lib.decode_attn_plan_splits(1, 8, 96, 10, sms, per) == -3
+    # one (b, kv-head) group per CTA already fills the GPU: no split
+    assert da.plan_splits(64, 8, 128, 32768, sms, per) == (1, 1)
+    # short prefix (16 tiles of 64 rows): one 16-CTA cluster per group, merged on chip
+    assert da.plan_splits(1, 16, 128, 1024, sms, per) == (16, 16)
+    # long prefixes: every resident CTA streams rows, merged through the workspace
+    assert da.plan_splits(1, 16, 128, 8192, sms, per) == (28, 1)
+    assert da.plan_splits(1, 8, 128, 32768, sms, per) == (57, 1)
+    assert da.plan_splits(8, 8, 128, 8192, sms, per) == (7, 1)
+    # without clusters a short prefix is split flat too
+    assert da.plan_splits(1, 16, 128, 1024, sms, per, cluster_max=1) == (16, 1)
+    # never more splits than tiles (64 rows at D=128, 128 at D=64)
+    assert da.plan_splits(1, 1, 128, 100, sms, per) == (2, 2)
+    assert da.plan_splits(1, 1, 64, 100, sms, per) == (1, 1)
+    assert da.plan_splits(1, 1, 128, 1, sms, per) == (1, 1)
+    # splits are whole clusters, fit one wave, and never shrink as the bound grows,
+    # so a workspace sized for the capacity fits any hint
+    for B, Hkv in [(1, 8), (1, 16), (2, 8), (8, 8), (4, 2), (3, 5)]:
+        prev = 0
+        for n in range(1, 40000, 397):
+            s, cs = da.plan_splits(B, Hkv, 128, n, sms, per)
+            assert s % cs == 0 and s >= prev and 1 <= cs <= 16
+            assert s == 1 or s * B * Hkv <= sms * per
+            prev = s
+    for bad in [(0, 8, 128, 10, sms, per, 16), (1, 0, 128, 10, sms, per, 16), (1, 8, 128, 0, sms, per, 16),
+                (1, 8, 128, 10, 0, per, 16), (1, 8, 128, 10, sms, 0, 16), (1, 8, 128, 10, sms, per, 0)]:
+        assert lib.decode_attn_plan_splits(*bad, None) == -2
+    assert lib.decode_attn_plan_splits(1, 8, 96, 10, sms, per, 16, None) == -3
 
 
 A = 0x10000  # a 16-byte-aligned address that is never dereferenced by these calls

@@ -222,6 +222,7 @@ def test_no_writes_outside_out_and_workspace():
     assert n > 0
     ws_buf = torch.full((n + 2 * 256,), 7, dtype=torch.uint8, device="cuda")
     ws = ws_buf[256:256 + n]
+    da.workspace_init(ws)
     da.kvcache_append(d.k_cache, d.v_cache, d.k_new, d.v_new, d.position_ids)
     da.decode_attn_fwd(d.q, d.k_cache, d.v_cache, d.kv_len.contiguous(), out=out, workspace=ws)
     torch.cuda.synchronize()
@@ -241,7 +242,8 @@ def test_side_stream(ora):
 
 
 def test_small_workspace_is_rejected():
-    step = W.long_context(seed=17, kv_len=4096, capacity=4096).to("cuda")
+    step = W.long_context(seed=17, kv_len=20000, capacity=20000).to("cuda")
+    assert da.decode_attn_workspace_size(1, 32, 8, 128, 20000) > 16
     with pytest.raises(da.DecodeAttnError) as e:
         da.decode_attn_fwd(step.q, step.k_cache, step.v_cache, step.kv_len.contiguous(),
                            workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
