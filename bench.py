@@ -176,7 +176,7 @@ class SweepStep:
         self.out = torch.empty((n, B, N_HEAD, HEAD_DIM), dtype=dt, device=device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         ws = max(da.decode_attn_workspace_size(B, N_HEAD, N_KV_HEAD, HEAD_DIM, kv) for kv in kv_lens)
-        self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
+        self.workspace = torch.zeros(max(ws, 16), dtype=torch.uint8, device=device)  # counters start at zero
         # (splits, cluster size) of each kv_len's calls
         self.splits = {kv: da.splits_for(B, N_HEAD, N_KV_HEAD, HEAD_DIM, kv, kv, dt) for kv in kv_lens}
 

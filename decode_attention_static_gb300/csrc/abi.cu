@@ -225,8 +225,11 @@ int decode_attn_plan_splits(int B, int n_kv_head, int head_dim, int max_kv_len, 
   const int64_t slots = (int64_t)num_sms * ctas_per_sm;  // CTAs resident at once
   const int rows = da::tile_rows(head_dim);
   const int64_t tiles = ((int64_t)max_kv_len + rows - 1) / rows;
-  // splits that fit one wave, at most one per tile
-  int64_t want = std::min<int64_t>({slots / units, tiles, (int64_t)da::kMaxSplits});
+  // Splits that fit one wave, at most one per tile. In a batch the lengths
+  // below the bound are unknown on the host; sizing for two waves keeps the
+  // long sequences' CTAs short while the short ones' extra splits exit at once.
+  const int64_t waves = B > 1 ? 2 : 1;
+  int64_t want = std::min<int64_t>({waves * slots / units, tiles, (int64_t)da::kMaxSplits});
   if (units > da::kMaxCounterGroups) want = 1;
   int64_t cs = 1;
   if (want >= 2) {

@@ -78,8 +78,8 @@ struct DecodeShape {
 template <int D, int G>
 struct DecodeConfig {
   static constexpr int kWarps = G >= 4 ? 8 : 16;
-  static constexpr int kPerLane = G >= 4 ? 8 : 16;
-  static constexpr bool kPackedK = G == 4;
+  static constexpr int kPerLane = G >= 8 ? 8 : 16;
+  static constexpr bool kPackedK = false;
   static constexpr int kStages = 6;
 };
 

@@ -87,8 +87,9 @@ DA_API int da_version(void);
  * n_kv_head KV heads, head_dim and a bound max_kv_len on the active length,
  * on a GPU with num_sms multiprocessors holding ctas_per_sm decode CTAs each,
  * where one thread-block cluster of up to cluster_max CTAs per group can be
- * resident. S is as many splits as fit one wave of resident CTAs, at most
- * one per tile of max_kv_len rows and at most 128. When each split would
+ * resident. S is as many splits as fit one wave of resident CTAs (two waves
+ * when B > 1, since most sequences of a batch are shorter than the bound),
+ * at most one per tile of max_kv_len rows and at most 128. When each split would
  * stream at most 4 tiles (a latency-bound short prefix) and cluster_max >= 2,
  * the splits of a group form one cluster of *cluster_size = S CTAs that
  * merge their partial softmax states through distributed shared memory;
