@@ -10,6 +10,7 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t* k_cache, uint8_t* 
                                                      int n_kv_head, int row_vecs, int capacity,
                                                      int32_t* err_flag) {
   pdl_wait();
+  pdl_trigger();  // the next grid may start its prologue while the rows are copied
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t total = (int64_t)B * n_kv_head * row_vecs;
   if (i >= total) return;

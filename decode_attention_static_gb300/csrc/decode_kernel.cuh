@@ -77,7 +77,7 @@ struct DecodeShape {
 // keeps enough bytes in flight to cover the loaded HBM latency.
 template <int D, int G>
 struct DecodeConfig {
-  static constexpr int kWarps = G >= 4 ? 8 : 16;
+  static constexpr int kWarps = 8;
   static constexpr int kPerLane = G >= 8 ? 8 : 16;
   static constexpr bool kPackedK = false;
   static constexpr int kStages = 6;
@@ -108,10 +108,15 @@ __device__ __forceinline__ void merge_warps(const float* red, int g, int d, floa
 // Arrival counter of one (b, g) group: zero before the call, each CTA of the
 // group adds one, the arrival that completes the count is the last one and
 // puts the counter back to zero for the next call. Returns 1 for the last.
+// The add is acquire-release at GPU scope: called by one thread after a CTA
+// barrier, it publishes every partial the CTA wrote before the barrier and,
+// for the last arrival, makes every other CTA's partials visible to the
+// threads that pass the next barrier (no separate fences).
 // A count already at or past `arrivals` means the counter was not zero: that
 // is reported as kErrWorkspace and the CTA does not merge.
 __device__ __forceinline__ int arrive_count(unsigned int* counter, int arrivals, int32_t* err_flag) {
-  const unsigned int before = atomicAdd(counter, 1u);
+  unsigned int before;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(before) : "l"(counter) : "memory");
   if (before + 1u < (unsigned int)arrivals) return 0;
   if (before + 1u > (unsigned int)arrivals) {
     if (err_flag) atomicOr(err_flag, kErrWorkspace);
@@ -278,66 +283,93 @@ __device__ __forceinline__ void consume_tile(const uint8_t* kt, const uint8_t* v
 
 // Final merge of the per-cluster partials of one group by the last CTA to
 // arrive: out = sum_k 2^(m_k - M) acc_k / sum_k 2^(m_k - M) l_k over the P
-// clusters. The weights of every (head, cluster) are computed once into
-// shared memory (`buf`, at least G * (P + 1) floats); then each thread owns
-// one output per pass and a 1/R share of the clusters (R = threads per
-// output), with its loads independent so that they are all in flight.
+// clusters. When the CTA has more threads than the group has outputs, R
+// threads share an output and each takes every R-th partial; otherwise each
+// thread takes KPT outputs. A thread loads a batch of partials of all its
+// outputs at once, (m, l) together with acc, and folds the batch into a
+// running (max, sum, acc): up to kBatch * R partials cost a single round trip
+// to L2. The R shares are combined through shared memory (`buf`, 3 * R * E
+// floats).
 template <typename T, int D, int G, int NT>
 __device__ __forceinline__ void merge_partials(const DecodeParams& p, int64_t head0, int P, int nc, float* buf) {
   constexpr int E = G * D;
-  float* wgt = buf;          // [G][P] weights
-  float* lsum = buf + G * P;  // [G]
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  for (int g = warp; g < G; g += NT / 32) {
-    const float* ml = p.ws_ml + (head0 + g) * nc * 2;
-    float mm = -INFINITY;
-    for (int k = lane; k < P; k += 32) mm = fmaxf(mm, __ldcg(ml + 2 * k));
+  constexpr int R = E >= NT ? 1 : NT / E;              // threads per output
+  constexpr int KPT = R > 1 ? 1 : (E + NT - 1) / NT;  // outputs per thread
+  constexpr int kBatch = KPT >= 4 ? 8 : 16;            // partials per output per round trip
+  const int r = R > 1 ? (int)threadIdx.x / E : 0;      // this thread's share of the partials
+  const bool active = r < R;
+  float mm[KPT], ls[KPT], as[KPT];
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, off));
-    float ls = 0.f;
-    for (int k = lane; k < P; k += 32) {
-      const float mk = __ldcg(ml + 2 * k);
-      const float w = (mk == -INFINITY) ? 0.f : fast_exp2(mk - mm);
-      wgt[g * P + k] = w;
-      ls = fmaf(__ldcg(ml + 2 * k + 1), w, ls);
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, off);
-    if (lane == 0) lsum[g] = ls;
+  for (int q = 0; q < KPT; ++q) {
+    mm[q] = -INFINITY;
+    ls[q] = 0.f;
+    as[q] = 0.f;
   }
-  __syncthreads();
-  constexpr int R = E >= NT ? 1 : NT / E;  // threads sharing one output
-  float* red = lsum + G;                   // [R][E] partial sums when R > 1
-  const int r = (int)threadIdx.x / E;      // this thread's share of the clusters (R > 1)
-  for (int i0 = 0; i0 < E; i0 += (R > 1 ? E : NT)) {
-    const int i = R > 1 ? (int)threadIdx.x % E : i0 + (int)threadIdx.x;
-    float as = 0.f;
-    if (i < E && r < R) {
-      const int g = i / D;
-      const float* part = p.ws_acc + (head0 + g) * nc * D + (i % D);
-      const float* w = wgt + g * P;
-      int k = R > 1 ? r : 0;
-      for (; k + 3 * R < P; k += 4 * R) {
-        const float v0 = __ldcg(part + (int64_t)k * D), v1 = __ldcg(part + (int64_t)(k + R) * D);
-        const float v2 = __ldcg(part + (int64_t)(k + 2 * R) * D), v3 = __ldcg(part + (int64_t)(k + 3 * R) * D);
-        as = fmaf(v0, w[k], as);
-        as = fmaf(v1, w[k + R], as);
-        as = fmaf(v2, w[k + 2 * R], as);
-        as = fmaf(v3, w[k + 3 * R], as);
+  for (int k0 = r; active && k0 < P; k0 += kBatch * R) {
+    float mv[KPT][kBatch], lv[KPT][kBatch], av[KPT][kBatch];
+#pragma unroll
+    for (int q = 0; q < KPT; ++q) {
+      const int i = R > 1 ? (int)threadIdx.x % E : (int)threadIdx.x + q * NT;
+      const int g = min(i, E - 1) / D;
+      const float* ml = p.ws_ml + (head0 + g) * nc * 2;
+      const float* part = p.ws_acc + (head0 + g) * nc * D + (min(i, E - 1) % D);
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int k = k0 + j * R;
+        const bool ok = i < E && k < P;
+        mv[q][j] = ok ? __ldcg(ml + 2 * k) : -INFINITY;
+        lv[q][j] = ok ? __ldcg(ml + 2 * k + 1) : 0.f;
+        av[q][j] = ok ? __ldcg(part + (int64_t)k * D) : 0.f;
       }
-      for (; k < P; k += R) as = fmaf(__ldcg(part + (int64_t)k * D), w[k], as);
     }
-    if (R > 1) {
-      if (r < R) red[r * E + i] = as;
-      __syncthreads();
-      if ((int)threadIdx.x < E) {
-        float t = 0.f;
-        for (int q = 0; q < R; ++q) t += red[q * E + threadIdx.x];
-        store_out<T>(p, head0 * D + threadIdx.x, t / lsum[threadIdx.x / D]);
+#pragma unroll
+    for (int q = 0; q < KPT; ++q) {
+      float mb = mm[q];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) mb = fmaxf(mb, mv[q][j]);
+      const float f = (mm[q] == -INFINITY) ? 0.f : fast_exp2(mm[q] - mb);
+      ls[q] *= f;
+      as[q] *= f;
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const float w = (mv[q][j] == -INFINITY) ? 0.f : fast_exp2(mv[q][j] - mb);
+        ls[q] = fmaf(lv[q][j], w, ls[q]);
+        as[q] = fmaf(av[q][j], w, as[q]);
       }
-    } else if (i < E) {
-      store_out<T>(p, head0 * D + i, as / lsum[i / D]);
+      mm[q] = mb;
+    }
+  }
+  if constexpr (R > 1) {
+    float* rm = buf;
+    float* rl = buf + R * E;
+    float* ra = buf + 2 * R * E;
+    if (active) {
+      const int i = (int)threadIdx.x % E;
+      rm[r * E + i] = mm[0];
+      rl[r * E + i] = ls[0];
+      ra[r * E + i] = as[0];
+    }
+    __syncthreads();
+    if ((int)threadIdx.x < E) {
+      const int i = threadIdx.x;
+      float M = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < R; ++q) M = fmaxf(M, rm[q * E + i]);
+      float L = 0.f, A = 0.f;
+#pragma unroll
+      for (int q = 0; q < R; ++q) {
+        const float mq = rm[q * E + i];
+        const float w = (mq == -INFINITY) ? 0.f : fast_exp2(mq - M);
+        L = fmaf(rl[q * E + i], w, L);
+        A = fmaf(ra[q * E + i], w, A);
+      }
+      store_out<T>(p, head0 * D + i, A / L);
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < KPT; ++q) {
+      const int i = (int)threadIdx.x + q * NT;
+      if (i < E) store_out<T>(p, head0 * D + i, as[q] / ls[q]);
     }
   }
 }
@@ -372,7 +404,6 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
   const int64_t head0 = (int64_t)b * H + (int64_t)g_kv * G;
   const int64_t kv_row0 = ((int64_t)b * p.n_kv_head + g_kv) * p.capacity;  // first cache row of this (b, g)
 
-  pdl_trigger();
   // Everything before pdl_wait() touches no memory the previous kernel on the
   // stream may still write, except for L2 prefetches (L2 is coherent).
   uint64_t policy = 0;
@@ -391,13 +422,19 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
     const int pr0 = s * ch;
     if (pr0 < lh) {
       const int rows = min(min(ch, lh - pr0), kStages * Shape::kTileRows);
-      const int64_t off = (kv_row0 + pr0) * Shape::kRowBytes;
-      prefetch_l2(p.k_cache + off, rows * Shape::kRowBytes);
-      prefetch_l2(p.v_cache + off, rows * Shape::kRowBytes);
+      for (int t0 = 0; t0 < rows; t0 += Shape::kTileRows) {
+        const int n = min(Shape::kTileRows, rows - t0);
+        const int64_t off = (kv_row0 + pr0 + t0) * Shape::kRowBytes;
+        prefetch_l2(p.k_cache + off, n * Shape::kRowBytes);
+        prefetch_l2(p.v_cache + off, n * Shape::kRowBytes);
+      }
     }
   }
   __syncthreads();
   pdl_wait();
+  // The next grid may be scheduled from here on: once it runs, every grid
+  // before this one has completed.
+  pdl_trigger();
 
   // Lane layout of the consumers: lane group `lrow` of a step takes one row;
   // within it, lane c holds vectors c + LPR * j (j < NV) of the row, slot j
@@ -680,7 +717,6 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
   if (nclusters > 1) {
     // Several clusters: the last CTA of the group to arrive merges the
     // cluster partials (written by other SMs, so read from L2).
-    __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
       const int last = arrive_count(p.counters + (int64_t)b * p.n_kv_head + g_kv, nclusters * CS, p.err_flag);
@@ -688,7 +724,6 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
     }
     __syncthreads();
     if (*reinterpret_cast<volatile int*>(last_flag)) {
-      __threadfence();
       // the ring is idle now; the cluster may still be reading `state`
       merge_partials<T, D, G, Shape::kThreads>(p, head0, nclusters, p.splits / CS, reinterpret_cast<float*>(smem));
     }
