@@ -178,6 +178,9 @@ int decode_common(const void* q, const void* k_cache, const void* v_cache, void*
   p.splits = splits;
   p.cluster = cluster;
   p.len_hint = bound;
+  // One sequence with an explicit bound: the bound is normally its length,
+  // so the kernel issues its first tiles before reading the length.
+  p.speculate = (B == 1 && max_kv_len_hint > 0) ? 1 : 0;
   p.qscale = scale * kLog2e;
   p.out = static_cast<uint8_t*>(out);
   if (need > 0) {

@@ -256,7 +256,8 @@ struct DecodeParams {
   const int32_t* lens;     // kv_len, or position_ids when lens_are_positions
   int lens_are_positions;
   int B, n_head, n_kv_head, capacity, splits;
-  int len_hint;            // host bound on the active lengths (<= capacity), for L2 prefetch only
+  int len_hint;            // host bound on the active lengths (<= capacity): L2 prefetch, early tiles
+  int speculate;           // 1: len_hint is expected to be the exact length (early tiles are issued)
   int cluster;             // CTAs per thread-block cluster along the split axis (divides splits)
   float qscale;            // softmax scale * log2(e)
   uint8_t* out;            // [B, n_head, D]

@@ -436,6 +436,53 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
   // before this one has completed.
   pdl_trigger();
 
+  const bool fused = p.k_new != nullptr;
+  const int64_t new_row = ((int64_t)b * p.n_kv_head + g_kv) * D;  // element offset into k_new
+  // Ring slot u takes rows [tr0, tr0 + rows) of this CTA's K and V, the row
+  // at Lx - 1 from k_new/v_new in the fused step (producer lane only).
+  auto issue = [&](int u, int tr0, int rows, int Lx) {
+    const int stage = u % kStages;
+    const bool new_last = fused && (tr0 + rows == Lx);
+    const int cached = new_last ? rows - 1 : rows;
+    uint8_t* kdst = smem + stage * Shape::kStageBytes;
+    uint8_t* vdst = kdst + kTileBytes;
+    mbar_arrive_expect_tx(&full[stage], 2u * rows * Shape::kRowBytes);
+    if (cached > 0) {
+      const int64_t off = (kv_row0 + tr0) * Shape::kRowBytes;
+      bulk_load(kdst, p.k_cache + off, cached * Shape::kRowBytes, &full[stage], policy);
+      bulk_load(vdst, p.v_cache + off, cached * Shape::kRowBytes, &full[stage], policy);
+    }
+    if (new_last) {
+      const int64_t off = new_row * 2;
+      bulk_load(kdst + cached * Shape::kRowBytes, p.k_new + off, Shape::kRowBytes, &full[stage], policy);
+      bulk_load(vdst + cached * Shape::kRowBytes, p.v_new + off, Shape::kRowBytes, &full[stage], policy);
+    }
+  };
+
+  // Early tiles: when the host's bound is expected to be the exact length
+  // (p.speculate), the producer issues this CTA's first tiles for that length
+  // before the length itself has been read. They are kept if the length
+  // matches, else left to land and discarded (ring slots 0..spec-1).
+  int spec = 0;
+  if (p.speculate) {
+    const int lh = p.len_hint;
+    const int chh = split_chunk(lh, p.splits, Shape::kTileRows);
+    const int r0h = min(s * chh, lh);
+    const int r1h = min(lh, r0h + chh);
+    spec = min((r1h - r0h + Shape::kTileRows - 1) / Shape::kTileRows, kStages);
+    if (threadIdx.x == CT) {
+      for (int t = 0; t < spec; ++t) {
+        const int tr0 = r0h + t * Shape::kTileRows;
+        issue(t, tr0, min(Shape::kTileRows, r1h - tr0), lh);
+      }
+    }
+  }
+  // A CTA leaving before its pipeline runs first lets the early tiles land.
+  auto drain_early = [&]() {
+    if (threadIdx.x == CT)
+      for (int t = 0; t < spec; ++t) mbar_wait(&full[t], 0);
+  };
+
   // Lane layout of the consumers: lane group `lrow` of a step takes one row;
   // within it, lane c holds vectors c + LPR * j (j < NV) of the row, slot j
   // visiting vector c + LPR * (j ^ swap).
@@ -461,19 +508,25 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
         reinterpret_cast<uint16_t*>(p.out)[head0 * D + i] = S::kNaN;
       if (threadIdx.x == 0 && p.err_flag) atomicOr(p.err_flag, err_bits);
     }
+    drain_early();
     return;
   }
   const int chunk = split_chunk(L, p.splits, Shape::kTileRows);
   const int nsplit = active_splits(L, chunk);
   const int nclusters = (nsplit + CS - 1) / CS;  // clusters with at least one active split
-  if (cid >= nclusters) return;                   // the whole cluster is idle
+  if (cid >= nclusters) {  // the whole cluster is idle
+    drain_early();
+    return;
+  }
   // Splits past nsplit in an active cluster read nothing and contribute an
   // empty state (m = -inf, l = 0), but take part in the cluster barriers.
   const int r0 = min(s * chunk, L);
   const int r1 = min(L, r0 + chunk);
   const int ntiles = (r1 - r0 + Shape::kTileRows - 1) / Shape::kTileRows;
-  const bool fused = p.k_new != nullptr;
-  const int64_t new_row = ((int64_t)b * p.n_kv_head + g_kv) * D;  // element offset into k_new
+  // Tile t sits in ring slot t + slot0: the early tiles are tiles 0..spec-1
+  // when the length matched the bound, else they occupy the first slots.
+  const bool keep = spec > 0 && L == p.len_hint;
+  const int slot0 = keep ? 0 : spec;
 
   if (warp == CW) {
     // ---------------- producer warp ----------------
@@ -486,39 +539,32 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
       *reinterpret_cast<uint4*>(p.v_cache_w + dst) = ld_global_nc_v4(p.v_new + src);
     }
     if (lane == 0) {
-      int issued = 0;
-      for (int t = 0; t < ntiles; ++t) {
-        const int stage = t % kStages;
-        if (t >= kStages) {
-          if (!mbar_wait(&empty[stage], ((t / kStages) & 1) ^ 1)) {
+      if (!keep) {
+        // Discarded early tiles: wait for them to land, then free their stages.
+        for (int t = 0; t < spec; ++t) {
+          if (!mbar_wait(&full[t], 0)) atomicOr(abort_flag, 1);
+          for (int w = 0; w < CW; ++w) mbar_arrive(&empty[t]);
+        }
+      }
+      int next = keep ? spec : slot0;  // next ring slot to fill
+      for (int t = keep ? spec : 0; t < ntiles; ++t) {
+        const int u = t + slot0;
+        const int stage = u % kStages;
+        if (u >= kStages) {
+          if (!mbar_wait(&empty[stage], ((u / kStages) & 1) ^ 1)) {
             atomicOr(abort_flag, 1);
             break;
           }
         }
         if (*reinterpret_cast<volatile int*>(abort_flag)) break;
         const int tr0 = r0 + t * Shape::kTileRows;
-        const int rows = min(Shape::kTileRows, r1 - tr0);
-        const bool new_last = fused && (tr0 + rows == L);
-        const int cached = new_last ? rows - 1 : rows;
-        uint8_t* kdst = smem + stage * Shape::kStageBytes;
-        uint8_t* vdst = kdst + kTileBytes;
-        mbar_arrive_expect_tx(&full[stage], 2u * rows * Shape::kRowBytes);
-        if (cached > 0) {
-          const int64_t off = (kv_row0 + tr0) * Shape::kRowBytes;
-          bulk_load(kdst, p.k_cache + off, cached * Shape::kRowBytes, &full[stage], policy);
-          bulk_load(vdst, p.v_cache + off, cached * Shape::kRowBytes, &full[stage], policy);
-        }
-        if (new_last) {
-          const int64_t off = new_row * 2;
-          bulk_load(kdst + cached * Shape::kRowBytes, p.k_new + off, Shape::kRowBytes, &full[stage], policy);
-          bulk_load(vdst + cached * Shape::kRowBytes, p.v_new + off, Shape::kRowBytes, &full[stage], policy);
-        }
-        ++issued;
+        issue(u, tr0, min(Shape::kTileRows, r1 - tr0), L);
+        next = u + 1;
       }
       // After an abort, let copies already in flight land before the CTA
-      // exits (bounded): the last tile issued to each stage.
+      // exits (bounded): the last slot filled in each stage.
       if (*reinterpret_cast<volatile int*>(abort_flag)) {
-        for (int t = max(0, issued - kStages); t < issued; ++t) mbar_wait(&full[t % kStages], (t / kStages) & 1);
+        for (int u = max(0, next - kStages); u < next; ++u) mbar_wait(&full[u % kStages], (u / kStages) & 1);
       }
     }
     __syncwarp();
@@ -549,9 +595,16 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
     }
 
     bool aborted = false;
-    for (int t = 0; t < ntiles; ++t) {
-      const int stage = t % kStages;
-      const bool ok_wait = mbar_wait(&full[stage], (t / kStages) & 1);
+    // Discarded early tiles: their copies must have landed (phase 0 of their
+    // stages) before this warp waits on a later phase of the same stages; a
+    // parity wait tells only the current phase from the one before it.
+    for (int t = 0; t < slot0; ++t) {
+      if (__any_sync(0xffffffffu, !mbar_wait(&full[t], 0))) aborted = true;
+    }
+    for (int t = 0; t < ntiles && !aborted; ++t) {
+      const int u = t + slot0;
+      const int stage = u % kStages;
+      const bool ok_wait = mbar_wait(&full[stage], (u / kStages) & 1);
       if (__any_sync(0xffffffffu, !ok_wait)) {
         aborted = true;
         break;

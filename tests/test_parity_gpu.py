@@ -131,6 +131,28 @@ def test_capacity_one_and_full(ora):
     check_step(ora, W.decode_step(2, 8, 2, 64, 777, "f16", [776, 776], seed=9), False, what="full capacity")
 
 
+@pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
+@pytest.mark.parametrize("kv_len", W.MHA_SWEEP_KV_LENS)
+def test_mha_sweep_exact_bound(ora, kv_len, fused):
+    """The length bound given as the exact length, as the benchmark calls it:
+    one sequence, so the first tiles are issued before the length is read."""
+    check_step(ora, W.mha_sweep(kv_len, seed=11), fused, hint=kv_len, what=f"MHA kv {kv_len} exact bound")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("D,H,Hkv", [(128, 16, 16), (128, 32, 8), (64, 8, 1)])
+def test_single_sequence_bounds(ora, dtype, D, H, Hkv):
+    """One sequence with a bound equal to, above and below its length: tiles
+    issued from the bound are kept only when it is exact, and discarded
+    otherwise (the NaN tail would show any discarded row that got used)."""
+    cap = 5000
+    for L in (1, 2, 63, 64, 65, 300, 1531, 4999):
+        step = W.decode_step(1, H, Hkv, D, cap, dtype, [L - 1], seed=L + D)
+        for hint in sorted({L, L + 1, L + 100, max(1, L - 1), cap}):
+            for fused in FUSED:
+                check_step(ora, step, fused, hint=hint, what=f"{dtype} D{D} H{H}/{Hkv} L{L} bound {hint} fused={fused}")
+
+
 @pytest.mark.parametrize("hint", [1, 64, 5000, 100000])
 def test_hint_only_sizes_the_launch(ora, hint):
     """Any max_kv_len_hint gives the same correct result, even one below the
