@@ -136,14 +136,12 @@ __device__ __forceinline__ void cluster_wait_acquire() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Load the float at the same shared-memory offset as `local` from the CTA of
+// Store a float at the same shared-memory offset as `local` in the CTA of
 // the given rank in this cluster (distributed shared memory).
-__device__ __forceinline__ float ld_cluster_f32(const float* local, int rank) {
+__device__ __forceinline__ void st_cluster_f32(float* local, int rank, float v) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
 // Programmatic dependent launch: wait for the preceding grid's memory, and

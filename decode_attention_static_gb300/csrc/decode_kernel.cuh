@@ -22,9 +22,10 @@
 //
 // Merge of the splits. The splits of one (b, g) group are launched as
 // thread-block clusters of `cluster` CTAs. Each CTA folds its warps' states
-// into one (m, l, acc) in shared memory; after a cluster barrier every CTA
-// merges a slice of the G x D outputs over all CTAs of its cluster by reading
-// their states through distributed shared memory. A group served by one
+// into one (m, l, acc) in shared memory and stores, through distributed
+// shared memory, each rank's slice of it into that rank; after one cluster
+// barrier every CTA merges its slice of the G x D outputs over all CTAs of
+// its cluster from its own shared memory. A group served by one
 // cluster writes `out` there and then; a group served by several clusters
 // writes one partial per cluster to the workspace, and the last CTA to
 // arrive (a per-group counter) merges those partials into `out`.
@@ -59,14 +60,17 @@ struct DecodeShape {
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kMergeFloats = CW * G * (D + 2);              // per-warp states
   static constexpr int kStateFloats = G * D + 2 * G;                 // CTA state: acc[G][D], m[G], l[G]
-  static constexpr int kMlFloats = kMaxCluster * 2 * G;              // (m, l) gathered from the cluster
-  static constexpr int kSmemBytes = kRingBytes + kMergeFloats * 4 + 2 * kStages * 8 + 16;
+  // Receive area of the cluster merge: (m, l) of up to kMaxCluster ranks and
+  // their shares of this CTA's slice of the outputs (at most G*D + 15 floats).
+  static constexpr int kRecvFloats = kMaxCluster * 2 * G + G * D + kMaxCluster;
+  static constexpr int kSmemBytes = kRingBytes + (kMergeFloats + kRecvFloats) * 4 + 2 * kStages * 8 + 16;
   static constexpr int kPerThread = (G * D + kConsumerThreads - 1) / kConsumerThreads;
   static_assert(DPL == 8 || DPL == 16, "8 or 16 elements per lane");
   static_assert(G <= kLanesPerRow, "the score reduction gives each head its own lanes");
   static_assert(kRowsPerWarp % kRowsPerStep == 0 && kSteps >= 1, "tile rows must split evenly over warps");
-  static_assert(kStateFloats + kMlFloats <= kMergeFloats, "the CTA state reuses the per-warp merge area");
-  static_assert((kMergeFloats * 4) % 8 == 0, "mbarriers need 8-byte alignment");
+  static_assert(kStateFloats <= kMergeFloats, "the CTA state reuses the per-warp merge area");
+  static_assert(((kMergeFloats + kRecvFloats) * 4) % 8 == 0, "mbarriers need 8-byte alignment");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
 };
 
 // Consumer warps, elements per lane, score arithmetic and ring depth of each
@@ -74,13 +78,14 @@ struct DecodeShape {
 // products with packed fp32x2 FMAs on fp32 q (fewer instructions when
 // G >= 4); otherwise one mixed-precision FMA per element and head on the raw
 // 16-bit values. One CTA per SM with a 6-stage ring of 32 KiB stages (192 KiB)
-// keeps enough bytes in flight to cover the loaded HBM latency.
+// keeps enough bytes in flight to cover the loaded HBM latency; G = 8 takes
+// 5 stages, its larger merge areas leaving no room for a sixth.
 template <int D, int G>
 struct DecodeConfig {
   static constexpr int kWarps = 8;
   static constexpr int kPerLane = G >= 8 ? 8 : 16;
   static constexpr bool kPackedK = false;
-  static constexpr int kStages = 6;
+  static constexpr int kStages = G >= 8 ? 5 : 6;
 };
 
 // Merge the per-warp (m, l, acc) states kept in shared memory for head g,
@@ -387,7 +392,8 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
   extern __shared__ __align__(128) uint8_t smem[];
   float* red = reinterpret_cast<float*>(smem + Shape::kRingBytes);
   float* state = red;                          // acc[G][D], m[G], l[G] of this CTA, written over red
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + Shape::kMergeFloats);
+  float* recv = red + Shape::kMergeFloats;     // receive area of the cluster merge
+  uint64_t* full = reinterpret_cast<uint64_t*>(recv + Shape::kRecvFloats);
   uint64_t* empty = full + kStages;
   int* abort_flag = reinterpret_cast<int*>(empty + kStages);
   int* last_flag = abort_flag + 1;
@@ -711,21 +717,30 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
   __syncthreads();
 
   // ---------------- merge over the cluster ----------------
-  // Each CTA merges a slice of the E outputs over the CS CTAs of its
-  // cluster, reading their states through distributed shared memory: first
-  // the (m, l) of every head of every rank (one load per thread), then for
-  // each output the CS accumulators (independent loads, all in flight).
-  float* mlbuf = state + Shape::kStateFloats;  // [cluster][2G]
-  if (CS > 1) {
-    cluster_arrive_release();
-    cluster_wait_acquire();
-    for (int t = threadIdx.x; t < CS * 2 * G; t += Shape::kThreads)
-      mlbuf[t] = ld_cluster_f32(state + E + t % (2 * G), t / (2 * G));
-    __syncthreads();
-  }
+  // Rank k of the cluster merges outputs [k * per, (k + 1) * per). Every CTA
+  // pushes its (m, l) and, for each rank, the slice of its accumulator that
+  // rank merges into that rank's receive area (distributed shared-memory
+  // stores, no round trips); after one cluster barrier each CTA merges its
+  // slice from its own shared memory. Nothing is read remotely, so a CTA
+  // may leave as soon as it has merged.
   const int per = (E + CS - 1) / CS;  // outputs merged by each CTA of the cluster
   const int e0 = rank * per;
   const int e1 = min(E, e0 + per);
+  float* ml_in = recv;                 // [CS][2G]: (m, l) of every rank
+  float* acc_in = recv + CS * 2 * G;   // [CS][per]: every rank's share of this CTA's slice
+  if (CS > 1) {
+    for (int t = threadIdx.x; t < CS * 2 * G; t += Shape::kThreads) {
+      const int k = t / (2 * G);
+      const int j = t - k * 2 * G;
+      st_cluster_f32(ml_in + rank * 2 * G + j, k, state[E + j]);
+    }
+    for (int i = threadIdx.x; i < E; i += Shape::kThreads) {
+      const int k = i / per;
+      st_cluster_f32(acc_in + rank * per + (i - k * per), k, state[i]);
+    }
+    cluster_arrive_release();
+    cluster_wait_acquire();
+  }
   for (int i = e0 + (int)threadIdx.x; i < e1; i += Shape::kThreads) {
     const int g = i / D;
     const int d = i % D;
@@ -735,22 +750,19 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
       ls = state[E + G + g];
       as = state[i];
     } else {
-      float a[kMaxCluster];
-#pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r) a[r] = r < CS ? ld_cluster_f32(state + i, r) : 0.f;
       mm = -INFINITY;
 #pragma unroll
       for (int r = 0; r < kMaxCluster; ++r)
-        if (r < CS) mm = fmaxf(mm, mlbuf[r * 2 * G + g]);
+        if (r < CS) mm = fmaxf(mm, ml_in[r * 2 * G + g]);
       ls = 0.f;
       as = 0.f;
 #pragma unroll
       for (int r = 0; r < kMaxCluster; ++r) {
         if (r < CS) {
-          const float mr = mlbuf[r * 2 * G + g];
+          const float mr = ml_in[r * 2 * G + g];
           const float f = (mr == -INFINITY) ? 0.f : fast_exp2(mr - mm);
-          ls = fmaf(mlbuf[r * 2 * G + G + g], f, ls);
-          as = fmaf(a[r], f, as);
+          ls = fmaf(ml_in[r * 2 * G + G + g], f, ls);
+          as = fmaf(acc_in[r * per + (i - e0)], f, as);
         }
       }
     }
@@ -765,7 +777,6 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
       }
     }
   }
-  if (CS > 1) cluster_arrive_release();  // this CTA is done reading the others' states
 
   if (nclusters > 1) {
     // Several clusters: the last CTA of the group to arrive merges the
@@ -777,11 +788,10 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
     }
     __syncthreads();
     if (*reinterpret_cast<volatile int*>(last_flag)) {
-      // the ring is idle now; the cluster may still be reading `state`
+      // the ring is idle now
       merge_partials<T, D, G, Shape::kThreads>(p, head0, nclusters, p.splits / CS, reinterpret_cast<float*>(smem));
     }
   }
-  if (CS > 1) cluster_wait_acquire();  // keep this CTA's state alive until the cluster has read it
 }
 
 }  // namespace da
