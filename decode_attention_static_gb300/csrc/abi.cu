@@ -236,13 +236,24 @@ int decode_attn_plan_splits(int B, int n_kv_head, int head_dim, int max_kv_len, 
   if (units > da::kMaxCounterGroups) want = 1;
   int64_t cs = 1;
   if (want >= 2) {
-    // Short prefixes are latency-bound: one cluster per group merges its
-    // splits on chip. Long ones are bandwidth-bound: spread the rows over
-    // every resident CTA and merge through the workspace.
-    const int64_t c = std::min<int64_t>({(int64_t)cluster_max, (int64_t)da::kMaxClusterSize, want});
-    if (c >= 2 && tiles <= da::kClusterTilesPerSplit * c) {
-      cs = c;
-      want = c;
+    const int64_t fit = std::min<int64_t>(cluster_max, da::kMaxClusterSize);
+    if (B == 1 && fit >= 2 && units * fit >= num_sms && tiles >= 2 * fit) {
+      // A long prefix of one sequence: one cluster of `fit` CTAs per group
+      // already covers every SM, and merges on chip instead of through L2.
+      cs = fit;
+    } else {
+      // A short prefix is latency-bound: one cluster per group, at most one
+      // CTA per SM, about ctas_per_sm tiles per CTA. Too short for two
+      // CTAs: no split at all.
+      const int64_t c = std::min<int64_t>(
+          {fit, std::max<int64_t>(1, num_sms / units), (tiles + ctas_per_sm - 1) / ctas_per_sm});
+      if (tiles <= da::kClusterTilesPerSplit * std::max<int64_t>(c, 1)) cs = c >= 2 ? c : 0;
+    }
+    if (cs > 1) {
+      want = cs;
+    } else if (cs == 0) {
+      want = 1;
+      cs = 1;
     }
   } else {
     want = 1;
@@ -254,8 +265,21 @@ int decode_attn_plan_splits(int B, int n_kv_head, int head_dim, int max_kv_len, 
 size_t decode_attn_workspace_size(int B, int n_head, int n_kv_head, int head_dim, int capacity) {
   if (da::check_sizes(B, n_head, n_kv_head, head_dim, capacity, DA_F16) != DA_OK) return (size_t)-1;
   if (B == 0) return 0;
+  // The plan depends on the length bound: take the largest need over the
+  // bounds of up to 4 * 16 tiles (where the short-prefix plans live) and
+  // the capacity (beyond those, flat splits only grow with the bound).
   size_t most = 0;
+  const int rows = da::tile_rows(head_dim);
   for (int dtype = DA_F16; dtype <= DA_BF16; ++dtype) {
+    for (int t = 1; t <= 4 * da::kMaxClusterSize + 1; ++t) {
+      const int bound = t * rows < capacity ? t * rows : capacity;
+      int splits = 1, cluster = 1;
+      if (da::plan_for_device(dtype, B, n_kv_head, head_dim, n_head / n_kv_head, bound, &splits, &cluster) !=
+          DA_OK)
+        return (size_t)-1;
+      most = std::max(most, da::workspace_bytes_for(B, n_head, splits, cluster, head_dim));
+      if (bound == capacity) break;
+    }
     int splits = 1, cluster = 1;
     if (da::plan_for_device(dtype, B, n_kv_head, head_dim, n_head / n_kv_head, capacity, &splits, &cluster) !=
         DA_OK)

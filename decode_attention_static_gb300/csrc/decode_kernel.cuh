@@ -58,18 +58,18 @@ struct DecodeShape {
   static constexpr bool kSwap = kVecs == 2 && kLanesPerRow * 16 < 128;
   static constexpr int kStageBytes = 2 * kTileBytes;                 // K tile then V tile
   static constexpr int kRingBytes = kStages * kStageBytes;
-  static constexpr int kMergeFloats = CW * G * (D + 2);              // per-warp states
+  static constexpr int kMergeFloats = CW * G * (D + 2);              // per-warp states (in the idle ring)
   static constexpr int kStateFloats = G * D + 2 * G;                 // CTA state: acc[G][D], m[G], l[G]
   // Receive area of the cluster merge: (m, l) of up to kMaxCluster ranks and
   // their shares of this CTA's slice of the outputs (at most G*D + 15 floats).
   static constexpr int kRecvFloats = kMaxCluster * 2 * G + G * D + kMaxCluster;
-  static constexpr int kSmemBytes = kRingBytes + (kMergeFloats + kRecvFloats) * 4 + 2 * kStages * 8 + 16;
+  static constexpr int kSmemBytes = kRingBytes + (kStateFloats + kRecvFloats) * 4 + 2 * kStages * 8 + 16;
   static constexpr int kPerThread = (G * D + kConsumerThreads - 1) / kConsumerThreads;
   static_assert(DPL == 8 || DPL == 16, "8 or 16 elements per lane");
   static_assert(G <= kLanesPerRow, "the score reduction gives each head its own lanes");
   static_assert(kRowsPerWarp % kRowsPerStep == 0 && kSteps >= 1, "tile rows must split evenly over warps");
-  static_assert(kStateFloats <= kMergeFloats, "the CTA state reuses the per-warp merge area");
-  static_assert(((kMergeFloats + kRecvFloats) * 4) % 8 == 0, "mbarriers need 8-byte alignment");
+  static_assert(kMergeFloats * 4 <= kRingBytes, "the per-warp states fit the ring");
+  static_assert(((kStateFloats + kRecvFloats) * 4) % 8 == 0, "mbarriers need 8-byte alignment");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
 };
 
@@ -77,15 +77,16 @@ struct DecodeShape {
 // instance. kPackedK: convert each K element once and form the G dot
 // products with packed fp32x2 FMAs on fp32 q (fewer instructions when
 // G >= 4); otherwise one mixed-precision FMA per element and head on the raw
-// 16-bit values. One CTA per SM with a 6-stage ring of 32 KiB stages (192 KiB)
-// keeps enough bytes in flight to cover the loaded HBM latency; G = 8 takes
-// 5 stages, its larger merge areas leaving no room for a sixth.
+// 16-bit values. A 3-stage ring of 32 KiB stages (96 KiB) per CTA covers the
+// loaded HBM latency and leaves room for two CTAs per SM: thread-block
+// clusters of up to 13 CTAs then fit once per group for 16 groups, and the
+// next launch's CTAs can be resident while this one drains.
 template <int D, int G>
 struct DecodeConfig {
   static constexpr int kWarps = 8;
   static constexpr int kPerLane = G >= 8 ? 8 : 16;
   static constexpr bool kPackedK = false;
-  static constexpr int kStages = G >= 8 ? 5 : 6;
+  static constexpr int kStages = 3;
 };
 
 // Merge the per-warp (m, l, acc) states kept in shared memory for head g,
@@ -390,9 +391,9 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
   constexpr int E = G * D;  // outputs of a group
 
   extern __shared__ __align__(128) uint8_t smem[];
-  float* red = reinterpret_cast<float*>(smem + Shape::kRingBytes);
-  float* state = red;                          // acc[G][D], m[G], l[G] of this CTA, written over red
-  float* recv = red + Shape::kMergeFloats;     // receive area of the cluster merge
+  float* red = reinterpret_cast<float*>(smem);  // per-warp states, once the ring is idle
+  float* state = reinterpret_cast<float*>(smem + Shape::kRingBytes);  // acc[G][D], m[G], l[G] of this CTA
+  float* recv = state + Shape::kStateFloats;   // receive area of the cluster merge
   uint64_t* full = reinterpret_cast<uint64_t*>(recv + Shape::kRecvFloats);
   uint64_t* empty = full + kStages;
   int* abort_flag = reinterpret_cast<int*>(empty + kStages);
@@ -670,7 +671,9 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
       }
     }
 
-    // Per-warp states to shared memory: red[warp][g][0..D) = acc, [D] = m, [D+1] = l.
+    // Per-warp states to shared memory, over the ring once every consumer
+    // warp is done with it: red[warp][g][0..D) = acc, [D] = m, [D+1] = l.
+    asm volatile("bar.sync 1, %0;" ::"n"(CT) : "memory");
     if (lrow == 0) {
 #pragma unroll
       for (int g = 0; g < G; ++g) {
@@ -700,7 +703,6 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
       const int i = threadIdx.x + k * CT;
       if (i < E) merge_warps<D, G, CW>(red, i / D, i % D, &vm[k], &vl[k], &va[k]);
     }
-    asm volatile("bar.sync 1, %0;" ::"n"(CT) : "memory");  // red is read; state overwrites it
     const float nan = __int_as_float(0x7fc00000);
 #pragma unroll
     for (int k = 0; k < Shape::kPerThread; ++k) {

@@ -87,13 +87,17 @@ DA_API int da_version(void);
  * n_kv_head KV heads, head_dim and a bound max_kv_len on the active length,
  * on a GPU with num_sms multiprocessors holding ctas_per_sm decode CTAs each,
  * where one thread-block cluster of up to cluster_max CTAs per group can be
- * resident. S is as many splits as fit one wave of resident CTAs (two waves
- * when B > 1, since most sequences of a batch are shorter than the bound),
- * at most one per tile of max_kv_len rows and at most 128. When each split would
- * stream at most 4 tiles (a latency-bound short prefix) and cluster_max >= 2,
- * the splits of a group form one cluster of *cluster_size = S CTAs that
- * merge their partial softmax states through distributed shared memory;
- * otherwise *cluster_size = 1 and the partials go through the workspace.
+ * resident. Flat plan: S is as many splits as fit one wave of resident CTAs
+ * (two waves when B > 1, since most sequences of a batch are shorter than the
+ * bound), at most one per tile of max_kv_len rows and at most 128; the
+ * partials go through the workspace (*cluster_size = 1). Cluster plans, where
+ * the S splits of a group form one cluster of *cluster_size = S CTAs that
+ * merge their partial softmax states through distributed shared memory:
+ * (a) one sequence whose clusters of c = min(cluster_max, 16) CTAs cover every
+ * SM (B * n_kv_head * c >= num_sms) over at least 2c tiles: S = c;
+ * (b) a short prefix: S = min(c, num_sms / (B * n_kv_head), tiles /
+ * ctas_per_sm rounded up) when each split then streams at most 4 tiles, and
+ * no split at all (S = 1) when that S is below 2.
  * (*cluster_size is written when non-NULL.) Each sequence b then splits its
  * own kv_len[b] rows evenly over at most S CTAs, in whole tiles.
  * Returns S >= 1, or a negative da_status.

@@ -56,17 +56,23 @@ def test_plan_splits_properties(lib):
     sms, per = 152, 3
     # one (b, kv-head) group per CTA already fills the GPU: no split
     assert da.plan_splits(64, 8, 128, 32768, sms, per) == (1, 1)
-    # short prefix (16 tiles of 64 rows): one 16-CTA cluster per group, merged on chip
-    assert da.plan_splits(1, 16, 128, 1024, sms, per) == (16, 16)
-    # long prefixes: every resident CTA streams rows, merged through the workspace
-    assert da.plan_splits(1, 16, 128, 8192, sms, per) == (28, 1)
+    # short prefix (16 tiles of 64 rows): one cluster per group, at most one
+    # CTA per SM (152 // 16 = 9) and about `per` tiles per CTA (16 / 3 -> 6)
+    assert da.plan_splits(1, 16, 128, 1024, sms, per) == (6, 6)
+    # long prefix of one sequence whose largest clusters cover every SM
+    # (16 groups x 16 >= 152): one cluster per group, merged on chip
+    assert da.plan_splits(1, 16, 128, 8192, sms, per) == (16, 16)
+    # long prefix whose clusters would leave SMs idle (8 x 16 < 152): every
+    # resident CTA streams rows, merged through the workspace
     assert da.plan_splits(1, 8, 128, 32768, sms, per) == (57, 1)
     # a batch: two waves' worth of splits (most sequences are shorter than the bound)
     assert da.plan_splits(8, 8, 128, 8192, sms, per) == (14, 1)
     # without clusters a short prefix is split flat too
     assert da.plan_splits(1, 16, 128, 1024, sms, per, cluster_max=1) == (16, 1)
-    # never more splits than tiles (64 rows at D=128, 128 at D=64)
-    assert da.plan_splits(1, 1, 128, 100, sms, per) == (2, 2)
+    # never more splits than tiles (64 rows at D=128, 128 at D=64); two tiles
+    # are too short to share between CTAs holding `per` tiles each
+    assert da.plan_splits(1, 1, 128, 100, sms, per) == (1, 1)
+    assert da.plan_splits(1, 1, 128, 100, sms, 1) == (2, 2)
     assert da.plan_splits(1, 1, 64, 100, sms, per) == (1, 1)
     assert da.plan_splits(1, 1, 128, 1, sms, per) == (1, 1)
     # splits are whole clusters, fit one wave, and never shrink as the bound grows,
