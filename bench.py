@@ -477,9 +477,163 @@ def run_ours(args) -> dict | None:
         "gpu_launches": step.launches_per_step() * args.steps,
         "clocks": clk,
     }
+    if not args.no_extras and rank == 0:
+        out["kv_curve"] = kv_curve(torch, da, device, step.l2_bytes)
+        out["configs"] = other_configs(torch, da, device, step.l2_bytes)
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     return out
+
+
+# ---------------------------------------------------------------------------
+# Other configurations, reported beside the headline sweep (not part of
+# `value`): the µs-vs-kv_len curve at the long-context shape and the other
+# workloads of the method, each timed as a CUDA graph of public calls.
+
+CURVE_KV = (256, 512, 1024, 2048, 4096, 8192, 16384, 32768)
+
+
+def graph_us_per_call(torch, device, issue, calls: int, reps: int, flush=None) -> float:
+    """µs per public call: `issue()` makes `calls` calls; it is captured once
+    in a CUDA graph and replayed `reps` times between CUDA events. With
+    `flush`, L2 is flushed before every replay, outside the timed events."""
+    issue()
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        issue()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize(device)
+    if flush is None:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize(device)
+        return a.elapsed_time(b) * 1e3 / (reps * calls)
+    total = 0.0
+    for _ in range(reps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize(device)
+        total += a.elapsed_time(b)
+    return total * 1e3 / (reps * calls)
+
+
+def kv_curve(torch, da, device, l2_bytes: int) -> list:
+    """Long-context shape (B=1, 32 query / 8 KV heads, head_dim 128, bf16),
+    fused append + attend per call, over rotating layer caches totalling at
+    least 3x L2, for each kv_len of CURVE_KV."""
+    H, Hkv, D, dt = 32, 8, 128, torch.bfloat16
+    gen = torch.Generator(device="cpu").manual_seed(11)
+    res = []
+    for kv in CURVE_KV:
+        per_layer = 2 * Hkv * kv * D * 2
+        layers = max(2, math.ceil(3 * l2_bytes / per_layer))
+        k = torch.empty(layers, 1, Hkv, kv, D, dtype=dt, device=device).normal_()
+        v = torch.empty_like(k).normal_()
+        q = torch.randn(layers, 1, H, D, generator=gen).to(dt).to(device)
+        kn = torch.randn(layers, 1, Hkv, D, generator=gen).to(dt).to(device)
+        vn = torch.randn(layers, 1, Hkv, D, generator=gen).to(dt).to(device)
+        out = torch.empty_like(q)
+        pos = torch.full((1,), kv - 1, dtype=torch.int32, device=device)
+        ws = da.alloc_workspace(1, H, Hkv, D, kv)
+
+        def issue():
+            for l in range(layers):
+                da.decode_step_fwd(q[l], k[l], v[l], kn[l], vn[l], pos, out=out[l], workspace=ws,
+                                   max_kv_len_hint=kv)
+
+        us = graph_us_per_call(torch, device, issue, layers, reps=max(3, 2000 // layers))
+        b = attend_bytes(1, H, Hkv, D, [kv], 2) + append_bytes(1, Hkv, D, 2)
+        s, cs = da.splits_for(1, H, Hkv, D, kv, kv, dt)
+        res.append({"kv_len": kv, "layers": layers, "splits": s, "cluster": cs, "us_per_layer_step": round(us, 3),
+                    "gbs": round(b / (us * 1e-6) / 1e9, 1)})
+        del k, v
+    return res
+
+
+def other_configs(torch, da, device, l2_bytes: int) -> dict:
+    """The tiny GQA step, the batched streaming step and S2-Pro-shaped
+    generation layer-steps (36 layers of 32 / 8 heads, bf16, capacity 32768)."""
+    from decode_attention_static_gb300 import workloads as W
+
+    res = {}
+    flush_buf = torch.empty(3 * l2_bytes // 4 + 1, dtype=torch.int32, device=device)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    # tiny GQA: one fused step, launch-bound
+    t = W.tiny_gqa(seed=0)
+    t_hint = int(t.position_ids.max()) + 1
+    t = t.to(device)
+    ws = da.alloc_workspace(t.B, t.n_head, t.n_kv_head, t.head_dim, t.capacity)
+
+    def issue_tiny():
+        for _ in range(64):
+            da.decode_step_fwd(t.q, t.k_cache, t.v_cache, t.k_new, t.v_new, t.position_ids, workspace=ws,
+                               max_kv_len_hint=t_hint)
+
+    res["tiny_gqa"] = {"us_per_layer_step": round(graph_us_per_call(torch, device, issue_tiny, 64, 50), 3)}
+
+    # batched streaming: B=8, 16 / 8 heads, capacity 8192, ragged lengths; three
+    # copies of the caches rotate so that consecutive calls read cold HBM
+    s0 = W.batched_streaming(seed=4)
+    hint = int(s0.position_ids.max()) + 1
+    kvs = (s0.position_ids + 1).tolist()
+    s0 = s0.to(device)
+    kc = [s0.k_cache] + [s0.k_cache.clone() for _ in range(2)]
+    vc = [s0.v_cache] + [s0.v_cache.clone() for _ in range(2)]
+    ws = da.alloc_workspace(s0.B, s0.n_head, s0.n_kv_head, s0.head_dim, s0.capacity)
+
+    def issue_batch():
+        for i in range(6):
+            da.decode_step_fwd(s0.q, kc[i % 3], vc[i % 3], s0.k_new, s0.v_new, s0.position_ids, workspace=ws,
+                               max_kv_len_hint=hint)
+
+    us = graph_us_per_call(torch, device, issue_batch, 6, 30)
+    b = attend_bytes(s0.B, s0.n_head, s0.n_kv_head, s0.head_dim, kvs, 2) + append_bytes(s0.B, s0.n_kv_head,
+                                                                                        s0.head_dim, 2)
+    res["batched_streaming"] = {"us_per_layer_step": round(us, 3), "gbs": round(b / (us * 1e-6) / 1e9, 1),
+                                "sum_kv_len": int(sum(kvs))}
+    del kc, vc, s0
+
+    # S2-Pro-shaped generation: every layer's step at three positions of the
+    # 400-step run (kv_len 235, 435, 634), as run (prefix warm in L2, as right
+    # after the previous step) and with L2 flushed before each 36-layer step
+    layers, H, Hkv, D, cap, dt = 36, 32, 8, 128, 32768, torch.bfloat16
+    k = torch.empty(layers, 1, Hkv, cap, D, dtype=dt, device=device).normal_()
+    v = torch.empty_like(k).normal_()
+    gen = torch.Generator(device="cpu").manual_seed(12)
+    q = torch.randn(layers, 1, H, D, generator=gen).to(dt).to(device)
+    kn = torch.randn(layers, 1, Hkv, D, generator=gen).to(dt).to(device)
+    vn = torch.randn(layers, 1, Hkv, D, generator=gen).to(dt).to(device)
+    out = torch.empty_like(q)
+    ws = da.alloc_workspace(1, H, Hkv, D, cap)
+    gen_res = []
+    for kv in (235, 435, 634):
+        pos = torch.full((1,), kv - 1, dtype=torch.int32, device=device)
+
+        def issue_s2():
+            for l in range(layers):
+                da.decode_step_fwd(q[l], k[l], v[l], kn[l], vn[l], pos, out=out[l], workspace=ws,
+                                   max_kv_len_hint=kv)
+
+        warm = graph_us_per_call(torch, device, issue_s2, layers, 50)
+        cold = graph_us_per_call(torch, device, issue_s2, layers, 20, flush=flush)
+        b = attend_bytes(1, H, Hkv, D, [kv], 2) + append_bytes(1, Hkv, D, 2)
+        gen_res.append({"kv_len": kv, "us_per_layer_step_as_run": round(warm, 3),
+                        "us_per_layer_step_l2_flushed": round(cold, 3),
+                        "gbs_l2_flushed": round(b / (cold * 1e-6) / 1e9, 1)})
+    res["s2pro_generation"] = gen_res
+    del k, v, flush_buf
+    return res
 
 
 # ---------------------------------------------------------------------------
@@ -526,9 +680,42 @@ def cpu_baseline(budget_s: float) -> dict:
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    return {"value": round(bytes_ * passes / el / 1e9, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+    value = bytes_ * passes / el / 1e9
+    passes1, t1 = 0, time.perf_counter()
+    while True:
+        oracle_pass(ora, items, N_HEAD, 1)
+        passes1 += 1
+        el1 = time.perf_counter() - t1
+        if el1 >= budget_s / 2:
+            break
+    return {"value": round(value, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "value_1_thread": round(bytes_ * passes1 / el1 / 1e9, 4), "cpu_model": cpu_model(),
             "sample": f"{passes} pass(es) of one layer-step per kv_len in {{1024, 4096, 8192}} (16 heads, append "
-                      f"+ attend) in {el:.1f} s, fp64 C oracle, OpenMP over query heads"}
+                      f"+ attend) in {el:.1f} s, fp64 C oracle, OpenMP over query heads; then {passes1} pass(es) "
+                      f"on one thread in {el1:.1f} s"}
+
+
+def cpu_model() -> str:
+    """The host CPU's model string (or architecture when none is published)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name:"):
+                name = line.split(":", 1)[1].strip()
+                if name and name != "-":
+                    return name
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in pathlib.Path("/proc/cpuinfo").read_text().splitlines():
+            key = line.split(":")[0].strip().lower()
+            if key in ("model name", "cpu model", "hardware"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+
+    return platform.machine() or "unknown"
 
 
 def run_reference(args) -> dict | None:
@@ -581,6 +768,8 @@ def main(argv=None):
                     help="kv_len values of the sweep to run (a subset gives a smaller case, e.g. for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the kv_len curve and the other configurations (reported beside the sweep)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
