@@ -225,3 +225,25 @@ def s2pro_generation(seed: int = 0, layers: int = 36, prompt: int = 234, steps: 
     v_new = randn((steps, layers, B, Hkv, D), dt, gen)
     return Generation(layers, B, H, Hkv, D, capacity, prompt, steps, dt, k_prefix, v_prefix, q,
                       k_new, v_new)
+
+
+def rope_tables(rows: int, head_dim: int, base: float = 10000.0) -> tuple[torch.Tensor, torch.Tensor]:
+    """Position-embedding tables of the usual rotary scheme, as a model hands
+    them to its attention: row p holds cos(p * w_i) and sin(p * w_i) for the
+    frequencies w_i = base^(-2i / head_dim), i < head_dim / 2, repeated for the
+    two halves of the head ([rows, head_dim] fp32, computed in fp64). Model
+    parameters and inputs, not the method's arithmetic."""
+    half = head_dim // 2
+    w = base ** (-torch.arange(half, dtype=torch.float64) * 2.0 / head_dim)
+    ang = torch.arange(rows, dtype=torch.float64)[:, None] * w[None, :]
+    ang = torch.cat([ang, ang], dim=1)
+    return torch.cos(ang).to(torch.float32), torch.sin(ang).to(torch.float32)
+
+
+def random_rope_tables(rows: int, head_dim: int, seed: int) -> tuple[torch.Tensor, torch.Tensor]:
+    """Tables with a random angle per (row, frequency), halves repeated: for
+    tests that want every rotation, not one frequency ladder."""
+    gen = generator(seed)
+    ang = torch.rand((rows, head_dim // 2), generator=gen, dtype=torch.float64) * (2 * torch.pi) - torch.pi
+    ang = torch.cat([ang, ang], dim=1)
+    return torch.cos(ang).to(torch.float32), torch.sin(ang).to(torch.float32)

@@ -25,6 +25,7 @@ DTYPE_CODES = {"f16": F16, "fp16": F16, "float16": F16, "bf16": BF16, "bfloat16"
 _u16p = ctypes.POINTER(ctypes.c_uint16)
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _f64p = ctypes.POINTER(ctypes.c_double)
+_f32p = ctypes.POINTER(ctypes.c_float)
 
 
 def dtype_code(dtype) -> int:
@@ -53,6 +54,11 @@ class Oracle:
         lib.oracle_kvcache_append.restype = ctypes.c_int
         lib.oracle_decode_bits.argtypes = [_u16p, ctypes.c_int64, ctypes.c_int, _f64p]
         lib.oracle_decode_bits.restype = ctypes.c_int
+        lib.oracle_encode_f32.argtypes = [_f32p, ctypes.c_int64, ctypes.c_int, _u16p]
+        lib.oracle_encode_f32.restype = ctypes.c_int
+        lib.oracle_rope.argtypes = [_u16p, _f32p, _f32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_int, _u16p]
+        lib.oracle_rope.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         self._lib = lib
@@ -76,6 +82,35 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"oracle_decode_bits returned {rc}")
         return out
+
+    def encode_f32(self, values, dtype) -> np.ndarray:
+        """fp32 values -> raw 16-bit storage, round to nearest even."""
+        v = np.ascontiguousarray(values, dtype=np.float32)
+        out = np.empty(v.shape, dtype=np.uint16)
+        rc = self._lib.oracle_encode_f32(v.ctypes.data_as(_f32p), v.size, dtype_code(dtype),
+                                         out.ctypes.data_as(_u16p))
+        if rc != 0:
+            raise ValueError(f"oracle_encode_f32 returned {rc}")
+        return out
+
+    def rope(self, x, cos_table, sin_table, position_ids, dtype) -> tuple[np.ndarray, int]:
+        """Rotary embedding of x [B, heads, D] (raw 16-bit) with the table rows
+        [rows, D] (fp32) at position_ids[b]; returns (rotated raw 16-bit, count
+        of out-of-range positions, whose rows are left zero)."""
+        x = self._u16(x)
+        c = np.ascontiguousarray(cos_table, dtype=np.float32)
+        sn = np.ascontiguousarray(sin_table, dtype=np.float32)
+        pos = np.ascontiguousarray(position_ids, dtype=np.int32)
+        B, heads, D = x.shape
+        if c.shape != sn.shape or c.ndim != 2 or c.shape[1] != D or pos.shape != (B,):
+            raise ValueError("inconsistent shapes")
+        out = np.zeros_like(x)
+        rc = self._lib.oracle_rope(x.ctypes.data_as(_u16p), c.ctypes.data_as(_f32p), sn.ctypes.data_as(_f32p),
+                                   pos.ctypes.data_as(_i32p), B, heads, D, c.shape[0], dtype_code(dtype),
+                                   out.ctypes.data_as(_u16p))
+        if rc < 0:
+            raise ValueError(f"oracle_rope returned {rc}")
+        return out, int(rc)
 
     def decode_attn(self, q, k_cache, v_cache, kv_len, n_head: int, n_kv_head: int, dtype,
                     scale: float | None = None, threads: int = 1) -> np.ndarray:

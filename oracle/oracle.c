@@ -208,3 +208,123 @@ int oracle_max_threads(void) {
   return 1;
 #endif
 }
+
+/*
+ * Rotary position embedding of the query and of the new key row, as the
+ * patched forward_step applies it before the append (VoxCPM issue #395,
+ * section 4.1: query_states, key_states = apply_rotary_pos_emb(query_states,
+ * key_states, cos, sin), with (cos, sin) the position embedding of the
+ * current position). The pages do not print apply_rotary_pos_emb; this takes
+ * the usual half-rotation form of the MiniCPM / Llama family:
+ *
+ *   out = x * cos + rotate_half(x) * sin,  rotate_half(x) = [-x[D/2:], x[:D/2]]
+ *
+ * with cos and sin given as rows of two tables [rows, head_dim] indexed by
+ * the sequence's position. The rotated vector is rounded to the storage type
+ * (round to nearest even), as the pages' tensors are. Because that rounding
+ * decides stored bits, the arithmetic is fixed exactly: the 16-bit x is
+ * widened to fp32 (exact), each product is rounded to fp32, their sum (or
+ * difference) is rounded to fp32 (no fused multiply-add), and that fp32 value
+ * is rounded once to fp16 or bf16.
+ */
+
+/* fp32 -> IEEE 754 binary16, round to nearest even, overflow to infinity.
+ * NaN becomes the quiet NaN 0x7E00. */
+static uint16_t encode_f16(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  const uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+  const uint32_t expo = (u >> 23) & 0xffu;
+  uint32_t mant = u & 0x7fffffu;
+  if (expo == 0xffu) return (uint16_t)(sign | (mant ? 0x7e00u : 0x7c00u));
+  /* value = (1.mant) * 2^(expo - 127) for normal fp32; binary16 has bias 15 */
+  const int e = (int)expo - 127;
+  if (e > 15) return (uint16_t)(sign | 0x7c00u);
+  if (e >= -14) {
+    /* normal half: keep 10 of the 23 fraction bits */
+    uint32_t h = ((uint32_t)(e + 15) << 10) | (mant >> 13);
+    const uint32_t rest = mant & 0x1fffu; /* 13 dropped bits */
+    if (rest > 0x1000u || (rest == 0x1000u && (h & 1u))) h += 1u; /* may carry into the exponent: fine */
+    return (uint16_t)(sign | h);
+  }
+  /* subnormal half (or zero): value / 2^-24 rounded to an integer */
+  if (expo == 0) return sign; /* fp32 zero or subnormal: far below half's smallest subnormal */
+  mant |= 0x800000u;          /* 24-bit significand, value = mant * 2^(e - 23) */
+  const int shift = -e - 1;   /* value / 2^-24 = mant * 2^(e + 1) = mant >> (-e - 1) */
+  if (shift > 24) return sign;
+  const uint32_t q = mant >> shift;
+  const uint32_t rem = mant & ((1u << shift) - 1u);
+  const uint32_t half = 1u << (shift - 1);
+  uint32_t h = q;
+  if (rem > half || (rem == half && (q & 1u))) h += 1u; /* 0x400 carries into the smallest normal */
+  return (uint16_t)(sign | h);
+}
+
+/* fp32 -> bfloat16 (the top half of an fp32), round to nearest even.
+ * NaN becomes the quiet NaN 0x7FC0. */
+static uint16_t encode_bf16(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x7fffffu)) return (uint16_t)(((u >> 16) & 0x8000u) | 0x7fc0u);
+  const uint32_t lower = u & 0xffffu;
+  uint32_t upper = u >> 16;
+  if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1u;
+  return (uint16_t)upper;
+}
+
+static uint16_t encode(float f, int dtype) { return dtype == ORACLE_F16 ? encode_f16(f) : encode_bf16(f); }
+
+/* fp32 -> 16-bit storage, exported for the tests of the encoders. */
+int oracle_encode_f32(const float* in, int64_t n, int dtype, uint16_t* out) {
+  if (!in || !out || n < 0 || (dtype != ORACLE_F16 && dtype != ORACLE_BF16)) return ORACLE_ERR_ARGS;
+  for (int64_t i = 0; i < n; ++i) out[i] = encode(in[i], dtype);
+  return ORACLE_OK;
+}
+
+/*
+ *   x            [B, heads, head_dim]   raw 16-bit values (head_dim even)
+ *   cos_table    [rows, head_dim]       fp32
+ *   sin_table    [rows, head_dim]       fp32
+ *   position_ids [B]                    row of the tables for sequence b
+ *   out          [B, heads, head_dim]   raw 16-bit values
+ * A position outside [0, rows) leaves that sequence's rows of `out`
+ * untouched and is counted. Returns that count, or a negative error.
+ */
+int oracle_rope(const uint16_t* x, const float* cos_table, const float* sin_table, const int32_t* position_ids,
+                int B, int heads, int head_dim, int rows, int dtype, uint16_t* out) {
+  if (!x || !cos_table || !sin_table || !position_ids || !out) return ORACLE_ERR_ARGS;
+  if (B < 0 || heads < 1 || head_dim < 2 || (head_dim & 1) || rows < 1) return ORACLE_ERR_ARGS;
+  if (dtype != ORACLE_F16 && dtype != ORACLE_BF16) return ORACLE_ERR_ARGS;
+  const int half = head_dim / 2;
+  int bad = 0;
+  for (int b = 0; b < B; ++b) {
+    const int p = position_ids[b];
+    if (p < 0 || p >= rows) {
+      ++bad;
+      continue;
+    }
+    const float* c = cos_table + (int64_t)p * head_dim;
+    const float* s = sin_table + (int64_t)p * head_dim;
+    for (int h = 0; h < heads; ++h) {
+      const uint16_t* xr = x + ((int64_t)b * heads + h) * head_dim;
+      uint16_t* o = out + ((int64_t)b * heads + h) * head_dim;
+      for (int d = 0; d < head_dim; ++d) {
+        const float xv = (float)decode(xr[d], dtype);
+        float r;
+        if (d < half) {
+          const float yv = (float)decode(xr[d + half], dtype); /* rotate_half: -x[d + D/2] */
+          const float a = xv * c[d];
+          const float bb = yv * s[d];
+          r = a - bb;
+        } else {
+          const float yv = (float)decode(xr[d - half], dtype); /* rotate_half: +x[d - D/2] */
+          const float a = xv * c[d];
+          const float bb = yv * s[d];
+          r = a + bb;
+        }
+        o[d] = encode(r, dtype);
+      }
+    }
+  }
+  return bad;
+}

@@ -348,6 +348,137 @@ def pin_invalid_kv_len_gives_nan_rows(ora):
     _assert_close(got[1:2], ref, 1e-12, 1e-13, "valid row")
 
 
+def pin_encoders_round_to_nearest_even(ora):
+    """fp32 -> fp16 / bf16 storage: every finite 16-bit value round-trips bit
+    for bit, random fp32 values round as numpy's float16 and torch's bfloat16
+    casts do (both round to nearest even), and the midpoint between two
+    neighbouring fp16 values goes to the one with an even last bit."""
+    allbits = np.arange(65536, dtype=np.uint16)
+    for name in ("f16", "bf16"):
+        vals = ora.decode_bits(allbits, name)
+        fin = np.isfinite(vals)
+        back = ora.encode_f32(vals[fin].astype(np.float32), name)
+        if not np.array_equal(back, allbits[fin]):
+            bad = np.nonzero(back != allbits[fin])[0][:4]
+            raise AssertionError(f"{name}: round trip differs at {allbits[fin][bad]}")
+    rng = np.random.default_rng(5)
+    x = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-9, 6, 20000),
+                        [6.0e4, 6.6e4, 7.0e4, -1e-7, 3e-8, 2.98e-8, 0.0, -0.0]]).astype(np.float32)
+    with np.errstate(over="ignore"):
+        ref16 = x.astype(np.float16).view(np.uint16)
+    if not np.array_equal(ora.encode_f32(x, "f16"), ref16):
+        raise AssertionError("f16 encoder differs from numpy's float16 cast")
+    refbf = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    if not np.array_equal(ora.encode_f32(x, "bf16"), refbf):
+        raise AssertionError("bf16 encoder differs from torch's bfloat16 cast")
+    a = np.arange(0x3c00, 0x3c40, dtype=np.uint16)  # consecutive fp16 values in [1, 2)
+    av = ora.decode_bits(a, "f16")
+    mid = ((av[:-1] + av[1:]) / 2).astype(np.float32)  # exact in fp32
+    want = np.where(a[:-1] % 2 == 0, a[:-1], a[1:])
+    if not np.array_equal(ora.encode_f32(mid, "f16"), want):
+        raise AssertionError("fp16 ties are not broken to even")
+    a = np.arange(0x3f80, 0x3fc0, dtype=np.uint16)  # consecutive bf16 values in [1, 2)
+    av = ora.decode_bits(a, "bf16")
+    mid = ((av[:-1] + av[1:]) / 2).astype(np.float32)
+    want = np.where(a[:-1] % 2 == 0, a[:-1], a[1:])
+    if not np.array_equal(ora.encode_f32(mid, "bf16"), want):
+        raise AssertionError("bf16 ties are not broken to even")
+
+
+def _rope_fp64(x64, c, s):
+    """The rotation in float64 on decoded values: x*cos + rotate_half(x)*sin."""
+    half = x64.shape[-1] // 2
+    rot = np.concatenate([-x64[..., half:], x64[..., :half]], axis=-1)
+    return x64 * c + rot * s
+
+
+def pin_rope_identity_and_quarter_turn(ora):
+    """cos = 1, sin = 0 leaves every bit in place; cos = 0, sin = 1 is
+    rotate_half exactly: [-x[D/2:], x[:D/2]] (a sign flip and a swap of the
+    halves, no rounding)."""
+    for dtype in ("f16", "bf16"):
+        for D in (64, 128):
+            x = _bits(W.randn((3, 4, D), dtype, W.generator(D)))
+            pos = np.array([0, 2, 1], np.int32)
+            one, zero = np.ones((3, D), np.float32), np.zeros((3, D), np.float32)
+            got, bad = ora.rope(x, one, zero, pos, dtype)
+            if bad or not np.array_equal(got, x):
+                raise AssertionError(f"{dtype} D{D}: identity rotation changed bits")
+            got, _ = ora.rope(x, zero, one, pos, dtype)
+            half = D // 2
+            want = np.concatenate([x[..., half:] ^ np.uint16(0x8000), x[..., :half]], axis=-1)
+            if not np.array_equal(got, want):
+                raise AssertionError(f"{dtype} D{D}: quarter turn is not rotate_half")
+
+
+def pin_rope_within_one_rounding_of_exact(ora):
+    """Random angles: the oracle's fp32 evaluation rounded to the storage
+    type lies within one unit in the last place of the exact rotation."""
+    for dtype, ulp_rel in (("f16", 2.0 ** -10), ("bf16", 2.0 ** -7)):
+        D = 128
+        c, s = W.random_rope_tables(16, D, seed=3)
+        xt = W.randn((4, 8, D), dtype, W.generator(4))
+        pos = np.array([0, 5, 15, 9], np.int32)
+        got, _ = ora.rope(_bits(xt), c.numpy(), s.numpy(), pos, dtype)
+        exact = _rope_fp64(_exact_f64(xt), c.numpy().astype(np.float64)[pos][:, None, :],
+                           s.numpy().astype(np.float64)[pos][:, None, :])
+        g = ora.decode_bits(got, dtype)
+        err = np.abs(g - exact)
+        tol = ulp_rel * np.maximum(np.abs(exact), 2.0 ** -14) * 1.01
+        if not np.all(err <= tol):
+            i = np.argmax(err / tol)
+            raise AssertionError(f"{dtype}: rotation off by {err.flat[i]:.3g} (tol {tol.flat[i]:.3g})")
+
+
+def pin_rope_preserves_pair_norms(ora):
+    """A rotation keeps the length of every (x[i], x[i + D/2]) pair."""
+    D = 64
+    c, s = W.random_rope_tables(8, D, seed=6)
+    xt = W.randn((2, 16, D), "f16", W.generator(7))
+    pos = np.array([3, 7], np.int32)
+    got, _ = ora.rope(_bits(xt), c.numpy(), s.numpy(), pos, "f16")
+    x = _exact_f64(xt)
+    g = ora.decode_bits(got, "f16")
+    n0 = x[..., :D // 2] ** 2 + x[..., D // 2:] ** 2
+    n1 = g[..., :D // 2] ** 2 + g[..., D // 2:] ** 2
+    if not np.allclose(n1, n0, rtol=4e-3, atol=1e-6):
+        raise AssertionError("pair norms not preserved")
+
+
+def pin_rope_scores_depend_on_relative_position(ora):
+    """With the frequency-ladder tables, <rope(q, m), rope(k, n)> depends only
+    on m - n: shifting both positions by the same amount keeps the score
+    (within the rounding of the stored vectors)."""
+    D = 128
+    c, s = W.rope_tables(600, D)
+    q = W.randn((1, 1, D), "f16", W.generator(8))
+    k = W.randn((1, 1, D), "f16", W.generator(9))
+
+    def score(m, n):
+        rq, _ = ora.rope(_bits(q), c.numpy(), s.numpy(), np.array([m], np.int32), "f16")
+        rk, _ = ora.rope(_bits(k), c.numpy(), s.numpy(), np.array([n], np.int32), "f16")
+        return float(np.dot(ora.decode_bits(rq, "f16").ravel(), ora.decode_bits(rk, "f16").ravel()))
+
+    scale = float(np.linalg.norm(_exact_f64(q)) * np.linalg.norm(_exact_f64(k)))
+    for m, n, t in ((10, 3, 200), (0, 0, 517), (250, 249, 300)):
+        a, b = score(m, n), score(m + t, n + t)
+        if abs(a - b) > 4e-3 * scale:
+            raise AssertionError(f"score({m},{n})={a} vs score({m + t},{n + t})={b}")
+    # and it does change with the distance
+    if abs(score(10, 3) - score(10, 9)) < 1e-3 * scale:
+        raise AssertionError("scores ignore the relative position")
+
+
+def pin_rope_position_bounds(ora):
+    """A position outside the tables is counted and its rows left untouched."""
+    D = 64
+    c, s = W.rope_tables(10, D)
+    x = _bits(W.randn((3, 2, D), "bf16", W.generator(10)))
+    got, bad = ora.rope(x, c.numpy(), s.numpy(), np.array([10, 4, -1], np.int32), "bf16")
+    if bad != 2 or np.any(got[0]) or np.any(got[2]) or not np.any(got[1]):
+        raise AssertionError("out-of-range positions not reported")
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 

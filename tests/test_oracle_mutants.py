@@ -35,6 +35,16 @@ MUTANTS = [
     ("append ignores V", "memcpy(v_cache + dst, v_new + src", "memcpy(v_cache + dst, k_new + src"),
     ("kv_len bound not checked", "if (L < 1 || L > capacity) {", "if (L < 1) {"),
     ("position bound not checked", "if (p < 0 || p >= capacity) {", "if (p < 0) {"),
+    ("rope partner sign flipped", "r = a - bb;", "r = a + bb;"),
+    ("rope partner index", "decode(xr[d + half], dtype); /* rotate_half", "decode(xr[d], dtype); /* rotate_half"),
+    ("rope sin replaced by cos", "const float bb = yv * s[d];\n          r = a - bb;",
+     "const float bb = yv * c[d];\n          r = a - bb;"),
+    ("rope table row ignored", "const float* c = cos_table + (int64_t)p * head_dim;",
+     "const float* c = cos_table;"),
+    ("rope position bound not checked", "if (p < 0 || p >= rows) {", "if (p < 0) {"),
+    ("f16 encoder truncates", "if (rest > 0x1000u || (rest == 0x1000u && (h & 1u))) h += 1u;", ""),
+    ("f16 encoder subnormal shift", "const int shift = -e - 1;", "const int shift = -e;"),
+    ("bf16 encoder ties away from zero", "(lower == 0x8000u && (upper & 1u))", "(lower == 0x8000u)"),
 ]
 
 
