@@ -54,6 +54,8 @@ _SIGNATURES = {
                                         _vp], _i),
     "decode_step_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _vp, ctypes.c_size_t,
                          _i, _i, _vp, _vp], _i),
+    "decode_step_rope_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _vp,
+                              ctypes.c_size_t, _i, _i, _vp, _vp], _i),
 }
 
 
@@ -232,6 +234,36 @@ def decode_step_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
                                         _ptr(workspace), workspace.numel(), int(max_kv_len_hint), _dtype_code(q),
                                         _ptr(err_flag), _stream(q))
     _check("decode_step_fwd", st)
+    return out
+
+
+def decode_step_rope_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, k_new: torch.Tensor,
+                         v_new: torch.Tensor, rope_cos: torch.Tensor, rope_sin: torch.Tensor,
+                         position_ids: torch.Tensor, out: torch.Tensor | None = None, scale: float | None = None,
+                         workspace: torch.Tensor | None = None, max_kv_len_hint: int = 0,
+                         err_flag: torch.Tensor | None = None) -> torch.Tensor:
+    """decode_step_fwd with the rotary embedding of q and k_new at
+    position_ids (tables rope_cos/rope_sin fp32 [rows, D], rows >= capacity)."""
+    if out is None:
+        out = torch.empty_like(q)
+    B, H, Hkv, D, cap = _attn_shapes(q, k_cache, v_cache, out)
+    for n, t in (("k_new", k_new), ("v_new", v_new), ("position_ids", position_ids), ("rope_cos", rope_cos),
+                 ("rope_sin", rope_sin)):
+        _cuda_contig(n, t)
+    _require(tuple(k_new.shape) == (B, Hkv, D) and v_new.shape == k_new.shape, "k_new/v_new must be [B, n_kv_head, D]")
+    _require(position_ids.dtype == torch.int32 and position_ids.numel() == B, "position_ids must be int32 [B]")
+    _require(rope_cos.dtype == torch.float32 and rope_sin.dtype == torch.float32 and rope_cos.dim() == 2
+             and rope_cos.shape == rope_sin.shape and rope_cos.shape[1] == D, "rope tables must be fp32 [rows, D]")
+    if scale is None:
+        scale = D ** -0.5
+    if workspace is None:
+        workspace = alloc_workspace(B, H, Hkv, D, cap, q.device)
+    st = load_library().decode_step_rope_fwd(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
+                                             _ptr(rope_cos), _ptr(rope_sin), rope_cos.shape[0], _ptr(position_ids),
+                                             B, H, Hkv, D, cap, float(scale), _ptr(out), _ptr(workspace),
+                                             workspace.numel(), int(max_kv_len_hint), _dtype_code(q),
+                                             _ptr(err_flag), _stream(q))
+    _check("decode_step_rope_fwd", st)
     return out
 
 

@@ -19,7 +19,8 @@ INCLUDE = ROOT / "include"
 BUILD_DIR = ROOT / "_build"
 LIBRARY = PKG / "libdecode_attn.so"
 
-SOURCES = ["abi.cu", "decode_f16.cu", "decode_bf16.cu", "append.cu", "static_scratch.cu"]
+SOURCES = ["abi.cu", "decode_f16.cu", "decode_bf16.cu", "decode_f16_rope.cu", "decode_bf16_rope.cu", "append.cu",
+           "static_scratch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          f"-I{INCLUDE}", f"-I{CSRC}"]

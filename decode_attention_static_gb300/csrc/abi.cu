@@ -19,8 +19,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct DeviceState {
   std::atomic<int> sms{0};
-  std::atomic<int> ready[2][2][4];  // [dtype][head_dim 64/128][log2 group]
-  DecodeKernelInfo info[2][2][4];
+  std::atomic<int> ready[4][2][4];  // [dtype + 2 * rotary][head_dim 64/128][log2 group]
+  DecodeKernelInfo info[4][2][4];
 };
 
 DeviceState g_devices[kMaxDevices];
@@ -70,24 +70,30 @@ bool decode_supported(int head_dim, int group) {
   return (head_dim == 64 || head_dim == 128) && (group == 1 || group == 2 || group == 4 || group == 8);
 }
 
-cudaError_t decode_kernel_info(int dtype, int head_dim, int group, int device, DecodeKernelInfo* info) {
+cudaError_t decode_kernel_info(int dtype, int head_dim, int group, int device, DecodeKernelInfo* info, bool rope) {
+  const int ki = dtype + (rope ? 2 : 0);
   const int di = head_dim == 128 ? 1 : 0;
   const int gi = group_index(group);
   DeviceState& st = g_devices[device];
-  if (st.ready[dtype][di][gi].load(std::memory_order_acquire)) {
-    *info = st.info[dtype][di][gi];
+  if (st.ready[ki][di][gi].load(std::memory_order_acquire)) {
+    *info = st.info[ki][di][gi];
     return cudaSuccess;
   }
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (!st.ready[dtype][di][gi].load(std::memory_order_acquire)) {
+  if (!st.ready[ki][di][gi].load(std::memory_order_acquire)) {
     DecodeKernelInfo k = {};
-    cudaError_t e = dtype == DA_F16 ? decode_info_f16(head_dim, group, &k) : decode_info_bf16(head_dim, group, &k);
+    cudaError_t e;
+    if (rope) {
+      e = dtype == DA_F16 ? decode_info_f16_rope(head_dim, group, &k) : decode_info_bf16_rope(head_dim, group, &k);
+    } else {
+      e = dtype == DA_F16 ? decode_info_f16(head_dim, group, &k) : decode_info_bf16(head_dim, group, &k);
+    }
     if (e != cudaSuccess) return e;
     if (k.ctas_per_sm < 1) return cudaErrorInvalidConfiguration;
-    st.info[dtype][di][gi] = k;
-    st.ready[dtype][di][gi].store(1, std::memory_order_release);
+    st.info[ki][di][gi] = k;
+    st.ready[ki][di][gi].store(1, std::memory_order_release);
   }
-  *info = st.info[dtype][di][gi];
+  *info = st.info[ki][di][gi];
   return cudaSuccess;
 }
 
@@ -95,6 +101,9 @@ cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int gr
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr.val.programmaticStreamSerializationAllowed = 1;
+  if (p.rope_cos)
+    return dtype == DA_F16 ? launch_decode_f16_rope(p, head_dim, group, stream, &attr)
+                           : launch_decode_bf16_rope(p, head_dim, group, stream, &attr);
   return dtype == DA_F16 ? launch_decode_f16(p, head_dim, group, stream, &attr)
                          : launch_decode_bf16(p, head_dim, group, stream, &attr);
 }
@@ -119,8 +128,16 @@ int plan_for_device(int dtype, int B, int n_kv_head, int head_dim, int group, in
   int device = 0, sms = 0;
   if (current_device(&device) != cudaSuccess) return DA_ERR_CUDA;
   if (device_sms(device, &sms) != cudaSuccess) return DA_ERR_CUDA;
-  DecodeKernelInfo info;
+  // One plan serves the plain and the rotary instances (so that a workspace
+  // sized for one fits the other): take the smaller occupancy of the two.
+  // Querying both also applies both instances' launch attributes.
+  DecodeKernelInfo info, info_rope;
   if (decode_kernel_info(dtype, head_dim, group, device, &info) != cudaSuccess) return DA_ERR_CUDA;
+  if (decode_kernel_info(dtype, head_dim, group, device, &info_rope, true) != cudaSuccess) return DA_ERR_CUDA;
+  info.ctas_per_sm = std::min(info.ctas_per_sm, info_rope.ctas_per_sm);
+  info.cluster_max = std::min(info.cluster_max, info_rope.cluster_max);
+  for (int c = 0; c <= kMaxClusterSize; ++c)
+    info.active_clusters[c] = std::min(info.active_clusters[c], info_rope.active_clusters[c]);
   // the largest cluster size of which one cluster per group is co-resident
   const int64_t units = (int64_t)B * n_kv_head;
   int fit = 1;
@@ -141,12 +158,19 @@ int plan_for_device(int dtype, int B, int n_kv_head, int head_dim, int group, in
 int decode_common(const void* q, const void* k_cache, const void* v_cache, void* k_cache_w, void* v_cache_w,
                   const void* k_new, const void* v_new, const int32_t* lens, int lens_are_positions, int B,
                   int n_head, int n_kv_head, int head_dim, int capacity, float scale, void* out, void* workspace,
-                  size_t workspace_bytes, int max_kv_len_hint, int dtype, int32_t* err_flag, void* stream) {
+                  size_t workspace_bytes, int max_kv_len_hint, int dtype, int32_t* err_flag, void* stream,
+                  const float* rope_cos = nullptr, const float* rope_sin = nullptr, int rope_rows = 0) {
   int rc = check_sizes(B, n_head, n_kv_head, head_dim, capacity, dtype);
   if (rc != DA_OK) return rc;
   if (B == 0) return DA_OK;
   if (!q || !k_cache || !v_cache || !lens || !out) return DA_ERR_NULL;
   if (lens_are_positions && (!k_new || !v_new)) return DA_ERR_NULL;
+  if ((rope_cos != nullptr) != (rope_sin != nullptr)) return DA_ERR_NULL;
+  if (rope_cos) {
+    if (!lens_are_positions) return DA_ERR_NULL;  // rotary embedding comes with the fused step only
+    if (rope_rows < capacity) return DA_ERR_SHAPE;
+    if (!aligned16(rope_cos) || !aligned16(rope_sin)) return DA_ERR_ALIGN;
+  }
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
       (k_new && !aligned16(k_new)) || (v_new && !aligned16(v_new)))
     return DA_ERR_ALIGN;
@@ -177,6 +201,9 @@ int decode_common(const void* q, const void* k_cache, const void* v_cache, void*
   p.capacity = capacity;
   p.splits = splits;
   p.cluster = cluster;
+  p.rope_cos = rope_cos;
+  p.rope_sin = rope_sin;
+  p.rope_rows = rope_rows;
   p.len_hint = bound;
   // One sequence with an explicit bound: the bound is normally its length,
   // so the kernel issues its first tiles before reading the length.
@@ -346,6 +373,17 @@ int decode_step_fwd(const void* q, void* k_cache, void* v_cache, const void* k_n
   return da::decode_common(q, k_cache, v_cache, k_cache, v_cache, k_new, v_new, position_ids, 1, B, n_head,
                            n_kv_head, head_dim, capacity, scale, out, workspace, workspace_bytes, max_kv_len_hint,
                            dtype, err_flag, stream);
+}
+
+int decode_step_rope_fwd(const void* q, void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                         const float* rope_cos, const float* rope_sin, int rope_rows, const int32_t* position_ids,
+                         int B, int n_head, int n_kv_head, int head_dim, int capacity, float scale, void* out,
+                         void* workspace, size_t workspace_bytes, int max_kv_len_hint, int dtype, int32_t* err_flag,
+                         void* stream) {
+  if (B > 0 && (!rope_cos || !rope_sin)) return DA_ERR_NULL;
+  return da::decode_common(q, k_cache, v_cache, k_cache, v_cache, k_new, v_new, position_ids, 1, B, n_head,
+                           n_kv_head, head_dim, capacity, scale, out, workspace, workspace_bytes, max_kv_len_hint,
+                           dtype, err_flag, stream, rope_cos, rope_sin, rope_rows);
 }
 
 }  // extern "C"

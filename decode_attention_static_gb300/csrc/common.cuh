@@ -242,6 +242,58 @@ struct Storage<__half> {
   static constexpr uint16_t kNaN = 0x7E00;
 };
 
+// Rotary position embedding of one 16-byte vector x (8 elements at columns
+// [8c, 8c + 8) of a head) given the vector y at the same place in the other
+// half of the head, and that row's cos and sin: x * cos - y * sin in the
+// first half, x * cos + y * sin in the second (x * cos + rotate_half(x) *
+// sin). Each product and the sum are rounded to fp32 separately (no fused
+// multiply-add), and the result once to the storage type.
+template <typename T>
+__device__ __forceinline__ uint4 rope_vec8(const uint4& x, const uint4& y, const float (&cs)[8], const float (&sn)[8],
+                                           bool first_half) {
+  float xf[8], yf[8];
+  Storage<T>::unpack(x, xf);
+  Storage<T>::unpack(y, yf);
+  uint16_t r[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float a = __fmul_rn(xf[e], cs[e]);
+    const float b = __fmul_rn(yf[e], sn[e]);
+    r[e] = Storage<T>::round(first_half ? __fsub_rn(a, b) : __fadd_rn(a, b));
+  }
+  uint4 v;
+  v.x = (uint32_t)r[0] | ((uint32_t)r[1] << 16);
+  v.y = (uint32_t)r[2] | ((uint32_t)r[3] << 16);
+  v.z = (uint32_t)r[4] | ((uint32_t)r[5] << 16);
+  v.w = (uint32_t)r[6] | ((uint32_t)r[7] << 16);
+  return v;
+}
+
+__device__ __forceinline__ uint4 shfl_xor_v4(const uint4& v, int mask) {
+  uint4 r;
+  r.x = __shfl_xor_sync(0xffffffffu, v.x, mask);
+  r.y = __shfl_xor_sync(0xffffffffu, v.y, mask);
+  r.z = __shfl_xor_sync(0xffffffffu, v.z, mask);
+  r.w = __shfl_xor_sync(0xffffffffu, v.w, mask);
+  return r;
+}
+
+// The 8 fp32 values at columns [col, col + 8) of row `row` of a table with
+// `width` columns (16-byte aligned).
+__device__ __forceinline__ void load_f32x8(const float* table, int64_t row, int width, int col, float (&out)[8]) {
+  const uint8_t* p = reinterpret_cast<const uint8_t*>(table + row * width + col);
+  const uint4 a = ld_global_nc_v4(p);
+  const uint4 b = ld_global_nc_v4(p + 16);
+  out[0] = __uint_as_float(a.x);
+  out[1] = __uint_as_float(a.y);
+  out[2] = __uint_as_float(a.z);
+  out[3] = __uint_as_float(a.w);
+  out[4] = __uint_as_float(b.x);
+  out[5] = __uint_as_float(b.y);
+  out[6] = __uint_as_float(b.z);
+  out[7] = __uint_as_float(b.w);
+}
+
 // Parameters shared by the decode and combine kernels.
 struct DecodeParams {
   const uint8_t* q;        // [B, n_head, D]
@@ -254,6 +306,9 @@ struct DecodeParams {
   const int32_t* lens;     // kv_len, or position_ids when lens_are_positions
   int lens_are_positions;
   int B, n_head, n_kv_head, capacity, splits;
+  const float* rope_cos;   // fused step with rotary embedding: tables [rope_rows, D] (else null)
+  const float* rope_sin;
+  int rope_rows;
   int len_hint;            // host bound on the active lengths (<= capacity): L2 prefetch, early tiles
   int speculate;           // 1: len_hint is expected to be the exact length (early tiles are issued)
   int cluster;             // CTAs per thread-block cluster along the split axis (divides splits)

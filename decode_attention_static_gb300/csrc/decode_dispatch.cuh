@@ -1,5 +1,6 @@
 // Instantiation and launch of the decode kernel for one storage type over
-// head_dim in {64, 128} and group size in {1, 2, 4, 8}.
+// head_dim in {64, 128} and group size in {1, 2, 4, 8}; RP selects the
+// instances of the fused step with rotary embedding.
 #pragma once
 
 #include "decode_kernel.cuh"
@@ -11,13 +12,13 @@ template <int D, int G>
 using ConfiguredShape = DecodeShape<D, G, DecodeConfig<D, G>::kWarps, DecodeConfig<D, G>::kPerLane,
                                     DecodeConfig<D, G>::kStages>;
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool RP>
 constexpr auto configured_kernel() {
   return decode_split_kernel<T, D, G, DecodeConfig<D, G>::kWarps, DecodeConfig<D, G>::kPerLane,
-                             DecodeConfig<D, G>::kPackedK, DecodeConfig<D, G>::kStages>;
+                             DecodeConfig<D, G>::kPackedK, DecodeConfig<D, G>::kStages, RP>;
 }
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool RP>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream, const cudaLaunchAttribute* pdl) {
   using Shape = ConfiguredShape<D, G>;
   cudaLaunchConfig_t cfg = {};
@@ -37,17 +38,17 @@ cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream, const cu
   }
   cfg.attrs = attrs;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, configured_kernel<T, D, G>(), p);
+  return cudaLaunchKernelEx(&cfg, configured_kernel<T, D, G, RP>(), p);
 }
 
 // Applies the shared-memory and cluster-size opt-ins for the current device
 // and reports the occupancy of one instance: resident CTAs per SM and the
 // largest cluster (16, else 8) of which at least one fits.
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool RP>
 cudaError_t decode_info_t(DecodeKernelInfo* info) {
   using Shape = ConfiguredShape<D, G>;
   const int smem = Shape::kSmemBytes;
-  auto* fn = configured_kernel<T, D, G>();
+  auto* fn = configured_kernel<T, D, G, RP>();
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -81,18 +82,18 @@ cudaError_t decode_info_t(DecodeKernelInfo* info) {
   return cudaSuccess;
 }
 
-#define DA_DISPATCH_GROUP(T, D, FN, ...)                 \
+#define DA_DISPATCH_GROUP(T, RP, D, FN, ...)             \
   switch (group) {                                       \
-    case 1: return FN<T, D, 1>(__VA_ARGS__);             \
-    case 2: return FN<T, D, 2>(__VA_ARGS__);             \
-    case 4: return FN<T, D, 4>(__VA_ARGS__);             \
-    case 8: return FN<T, D, 8>(__VA_ARGS__);             \
+    case 1: return FN<T, D, 1, RP>(__VA_ARGS__);         \
+    case 2: return FN<T, D, 2, RP>(__VA_ARGS__);         \
+    case 4: return FN<T, D, 4, RP>(__VA_ARGS__);         \
+    case 8: return FN<T, D, 8, RP>(__VA_ARGS__);         \
     default: return cudaErrorInvalidValue;               \
   }
 
-#define DA_DISPATCH(T, FN, ...)                                         \
-  if (head_dim == 128) { DA_DISPATCH_GROUP(T, 128, FN, __VA_ARGS__) }   \
-  if (head_dim == 64) { DA_DISPATCH_GROUP(T, 64, FN, __VA_ARGS__) }     \
+#define DA_DISPATCH(T, RP, FN, ...)                                         \
+  if (head_dim == 128) { DA_DISPATCH_GROUP(T, RP, 128, FN, __VA_ARGS__) }   \
+  if (head_dim == 64) { DA_DISPATCH_GROUP(T, RP, 64, FN, __VA_ARGS__) }     \
   return cudaErrorInvalidValue;
 
 }  // namespace da

@@ -5,11 +5,11 @@ namespace da {
 
 cudaError_t launch_decode_f16(const DecodeParams& p, int head_dim, int group, cudaStream_t stream,
                               const cudaLaunchAttribute* attr) {
-  DA_DISPATCH(__half, launch_decode_t, p, stream, attr)
+  DA_DISPATCH(__half, false, launch_decode_t, p, stream, attr)
 }
 
 cudaError_t decode_info_f16(int head_dim, int group, DecodeKernelInfo* info) {
-  DA_DISPATCH(__half, decode_info_t, info)
+  DA_DISPATCH(__half, false, decode_info_t, info)
 }
 
 }  // namespace da

@@ -63,13 +63,17 @@ struct DecodeShape {
   // Receive area of the cluster merge: (m, l) of up to kMaxCluster ranks and
   // their shares of this CTA's slice of the outputs (at most G*D + 15 floats).
   static constexpr int kRecvFloats = kMaxCluster * 2 * G + G * D + kMaxCluster;
-  static constexpr int kSmemBytes = kRingBytes + (kStateFloats + kRecvFloats) * 4 + 2 * kStages * 8 + 16;
+  // Layout after the ring: CTA state, receive area, then the mbarriers and
+  // flags.
+  static constexpr int kBarOffset = (kRingBytes + (kStateFloats + kRecvFloats) * 4 + 7) / 8 * 8;
+  static constexpr int kSmemBytes = kBarOffset + 2 * kStages * 8 + 16;
   static constexpr int kPerThread = (G * D + kConsumerThreads - 1) / kConsumerThreads;
   static_assert(DPL == 8 || DPL == 16, "8 or 16 elements per lane");
   static_assert(G <= kLanesPerRow, "the score reduction gives each head its own lanes");
   static_assert(kRowsPerWarp % kRowsPerStep == 0 && kSteps >= 1, "tile rows must split evenly over warps");
   static_assert(kMergeFloats * 4 <= kRingBytes, "the per-warp states fit the ring");
-  static_assert(((kStateFloats + kRecvFloats) * 4) % 8 == 0, "mbarriers need 8-byte alignment");
+  static_assert(kBarOffset % 8 == 0, "mbarriers need 8-byte alignment");
+  static_assert(kVecs == 1, "one 16-byte vector per lane (rotary embedding pairs lanes c and c ^ D/16)");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
 };
 
@@ -382,7 +386,7 @@ __device__ __forceinline__ void merge_partials(const DecodeParams& p, int64_t he
   }
 }
 
-template <typename T, int D, int G, int CW, int DPL, bool PK, int NS>
+template <typename T, int D, int G, int CW, int DPL, bool PK, int NS, bool RP>
 __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const DecodeParams p) {
   using Shape = DecodeShape<D, G, CW, DPL, NS>;
   constexpr int kStages = NS;
@@ -396,7 +400,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
   float* red = reinterpret_cast<float*>(smem);  // per-warp states, once the ring is idle
   float* state = reinterpret_cast<float*>(smem + Shape::kRingBytes);  // acc[G][D], m[G], l[G] of this CTA
   float* recv = state + Shape::kStateFloats;   // receive area of the cluster merge
-  uint64_t* full = reinterpret_cast<uint64_t*>(recv + Shape::kRecvFloats);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Shape::kBarOffset);
   uint64_t* empty = full + kStages;
   int* abort_flag = reinterpret_cast<int*>(empty + kStages);
   int* last_flag = abort_flag + 1;
@@ -446,6 +450,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
   pdl_trigger();
 
   const bool fused = p.k_new != nullptr;
+  const bool rope = RP && fused && p.rope_cos != nullptr;  // instances with RP serve the rotary step
   const int64_t new_row = ((int64_t)b * p.n_kv_head + g_kv) * D;  // element offset into k_new
   // Ring slot u takes rows [tr0, tr0 + rows) of this CTA's K and V, the row
   // at Lx - 1 from k_new/v_new in the fused step (producer lane only).
@@ -455,17 +460,50 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
     const int cached = new_last ? rows - 1 : rows;
     uint8_t* kdst = smem + stage * Shape::kStageBytes;
     uint8_t* vdst = kdst + kTileBytes;
-    mbar_arrive_expect_tx(&full[stage], 2u * rows * Shape::kRowBytes);
+    // With rotary embedding the producer warp has already stored the new row
+    // into this stage (rope_row): only the cached rows arrive by TMA.
+    mbar_arrive_expect_tx(&full[stage], 2u * (new_last && rope ? cached : rows) * Shape::kRowBytes);
     if (cached > 0) {
       const int64_t off = (kv_row0 + tr0) * Shape::kRowBytes;
       bulk_load(kdst, p.k_cache + off, cached * Shape::kRowBytes, &full[stage], policy);
       bulk_load(vdst, p.v_cache + off, cached * Shape::kRowBytes, &full[stage], policy);
     }
-    if (new_last) {
+    if (new_last && !rope) {
       const int64_t off = new_row * 2;
       bulk_load(kdst + cached * Shape::kRowBytes, p.k_new + off, Shape::kRowBytes, &full[stage], policy);
       bulk_load(vdst + cached * Shape::kRowBytes, p.v_new + off, Shape::kRowBytes, &full[stage], policy);
     }
+  };
+
+  // Fused step with rotary embedding: the whole producer warp rotates the new
+  // key row for position `pos` (lanes < D/8 hold one 16-byte vector each;
+  // lane c pairs with lane c ^ D/16, the same columns in the other half) and
+  // stores it, with the V row, as row `at` of the (free) stage of ring slot
+  // u, before lane 0 issues that slot: the __syncwarp and lane 0's mbarrier
+  // arrive (release) order these stores before the consumers' wait. With
+  // `to_cache` it also writes the rows into the cache at `pos`.
+  auto rope_row = [&](int pos, int u, int at, bool to_cache) {
+    uint4 kx = make_uint4(0u, 0u, 0u, 0u), vx = kx;
+    float cs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, sn[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (lane < D / 8) {
+      kx = ld_global_nc_v4(p.k_new + (new_row + lane * 8) * 2);
+      vx = ld_global_nc_v4(p.v_new + (new_row + lane * 8) * 2);
+      load_f32x8(p.rope_cos, pos, D, lane * 8, cs);
+      load_f32x8(p.rope_sin, pos, D, lane * 8, sn);
+    }
+    const uint4 ky = shfl_xor_v4(kx, D / 16);
+    if (lane < D / 8) {
+      const uint4 kr = rope_vec8<T>(kx, ky, cs, sn, lane < D / 16);
+      uint8_t* kdst = smem + (u % kStages) * Shape::kStageBytes + at * Shape::kRowBytes + lane * 16;
+      *reinterpret_cast<uint4*>(kdst) = kr;
+      *reinterpret_cast<uint4*>(kdst + kTileBytes) = vx;
+      if (to_cache) {
+        const int64_t dst = (kv_row0 + pos) * Shape::kRowBytes + lane * 16;
+        *reinterpret_cast<uint4*>(p.k_cache_w + dst) = kr;
+        *reinterpret_cast<uint4*>(p.v_cache_w + dst) = vx;
+      }
+    }
+    __syncwarp();
   };
 
   // Early tiles: when the host's bound is expected to be the exact length
@@ -473,16 +511,22 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
   // before the length itself has been read. They are kept if the length
   // matches, else left to land and discarded (ring slots 0..spec-1).
   int spec = 0;
+  int spec_new = -1;  // early slot holding the rotated row of the bound's last position
   if (p.speculate) {
     const int lh = p.len_hint;
     const int chh = split_chunk(lh, p.splits, Shape::kTileRows);
     const int r0h = min(s * chh, lh);
     const int r1h = min(lh, r0h + chh);
     spec = min((r1h - r0h + Shape::kTileRows - 1) / Shape::kTileRows, kStages);
-    if (threadIdx.x == CT) {
+    if (warp == CW) {
       for (int t = 0; t < spec; ++t) {
         const int tr0 = r0h + t * Shape::kTileRows;
-        issue(t, tr0, min(Shape::kTileRows, r1h - tr0), lh);
+        const int rows = min(Shape::kTileRows, r1h - tr0);
+        if (rope && tr0 + rows == lh) {
+          rope_row(lh - 1, t, rows - 1, false);  // not into the cache before the length is known
+          spec_new = t;
+        }
+        if (lane == 0) issue(t, tr0, rows, lh);
       }
     }
   }
@@ -505,6 +549,15 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
 #pragma unroll
       for (int j = 0; j < NV; ++j)
         qraw[g][j] = ld_global_nc_v4(p.q + ((head0 + g) * D + (c + LPR * (j ^ swap)) * 8) * 2);
+  }
+  // Rotary embedding of q: the consumers fetch cos and sin of their columns
+  // for the bound's position now, and again below if the length differs.
+  float qcos[8], qsin[8];
+  int qpos = -1;
+  if (rope && warp < CW && p.speculate) {
+    qpos = p.len_hint - 1;
+    load_f32x8(p.rope_cos, qpos, D, c * 8, qcos);
+    load_f32x8(p.rope_sin, qpos, D, c * 8, qsin);
   }
 
   int32_t err_bits = 0;
@@ -536,10 +589,20 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
   // when the length matched the bound, else they occupy the first slots.
   const bool keep = spec > 0 && L == p.len_hint;
   const int slot0 = keep ? 0 : spec;
+  if (rope && warp < CW) {
+    if (qpos != L - 1) {
+      qpos = L - 1;
+      load_f32x8(p.rope_cos, qpos, D, c * 8, qcos);
+      load_f32x8(p.rope_sin, qpos, D, c * 8, qsin);
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) qraw[g][0] = rope_vec8<T>(qraw[g][0], shfl_xor_v4(qraw[g][0], LPR / 2), qcos, qsin,
+                                                          c < LPR / 2);
+  }
 
   if (warp == CW) {
     // ---------------- producer warp ----------------
-    if (fused && s == 0 && lane < D / 8) {
+    if (fused && !rope && s == 0 && lane < D / 8) {
       // The new row goes into the cache; no CTA of this launch reads it back
       // from there (the CTA owning row L-1 takes it from k_new/v_new).
       const int64_t dst = (kv_row0 + (L - 1)) * Shape::kRowBytes + lane * 16;
@@ -547,15 +610,45 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
       *reinterpret_cast<uint4*>(p.k_cache_w + dst) = ld_global_nc_v4(p.k_new + src);
       *reinterpret_cast<uint4*>(p.v_cache_w + dst) = ld_global_nc_v4(p.v_new + src);
     }
-    if (lane == 0) {
-      if (!keep) {
-        // Discarded early tiles: wait for them to land, then free their stages.
-        for (int t = 0; t < spec; ++t) {
-          if (!mbar_wait(&full[t], 0)) atomicOr(abort_flag, 1);
-          for (int w = 0; w < CW; ++w) mbar_arrive(&empty[t]);
-        }
+    if (lane == 0 && !keep) {
+      // Discarded early tiles: wait for them to land, then free their stages.
+      for (int t = 0; t < spec; ++t) {
+        if (!mbar_wait(&full[t], 0)) atomicOr(abort_flag, 1);
+        for (int w = 0; w < CW; ++w) mbar_arrive(&empty[t]);
       }
-      int next = keep ? spec : slot0;  // next ring slot to fill
+    }
+    __syncwarp();
+    if (keep && spec_new >= 0 && lane < D / 8) {
+      // The kept early slot spec_new holds the rotated row of position L - 1
+      // (its stage is not reused before the loop below): it goes into the
+      // cache now. No CTA of this launch reads that row back from the cache.
+      const uint8_t* src = smem + (spec_new % kStages) * Shape::kStageBytes +
+                           ((L - 1) - (r0 + spec_new * Shape::kTileRows)) * Shape::kRowBytes + lane * 16;
+      const int64_t dst = (kv_row0 + (L - 1)) * Shape::kRowBytes + lane * 16;
+      *reinterpret_cast<uint4*>(p.k_cache_w + dst) = *reinterpret_cast<const uint4*>(src);
+      *reinterpret_cast<uint4*>(p.v_cache_w + dst) = *reinterpret_cast<const uint4*>(src + kTileBytes);
+    }
+    int next = keep ? spec : slot0;  // next ring slot to fill
+    if constexpr (RP) {
+      // The whole warp walks the slots (lane 0 waits and issues) so that it
+      // can store the rotated row into a stage right before it is issued.
+      for (int t = keep ? spec : 0; t < ntiles; ++t) {
+        const int u = t + slot0;
+        const int stage = u % kStages;
+        int ok = 1;
+        if (lane == 0) {
+          if (u >= kStages && !mbar_wait(&empty[stage], ((u / kStages) & 1) ^ 1)) atomicOr(abort_flag, 1);
+          ok = *reinterpret_cast<volatile int*>(abort_flag) == 0;
+        }
+        __syncwarp();
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        const int tr0 = r0 + t * Shape::kTileRows;
+        const int rows = min(Shape::kTileRows, r1 - tr0);
+        if (rope && tr0 + rows == L) rope_row(L - 1, u, rows - 1, true);
+        if (lane == 0) issue(u, tr0, rows, L);
+        next = u + 1;
+      }
+    } else if (lane == 0) {
       for (int t = keep ? spec : 0; t < ntiles; ++t) {
         const int u = t + slot0;
         const int stage = u % kStages;
@@ -570,11 +663,11 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
         issue(u, tr0, min(Shape::kTileRows, r1 - tr0), L);
         next = u + 1;
       }
-      // After an abort, let copies already in flight land before the CTA
-      // exits (bounded): the last slot filled in each stage.
-      if (*reinterpret_cast<volatile int*>(abort_flag)) {
-        for (int u = max(0, next - kStages); u < next; ++u) mbar_wait(&full[u % kStages], (u / kStages) & 1);
-      }
+    }
+    // After an abort, let copies already in flight land before the CTA
+    // exits (bounded): the last slot filled in each stage.
+    if (lane == 0 && *reinterpret_cast<volatile int*>(abort_flag)) {
+      for (int u = max(0, next - kStages); u < next; ++u) mbar_wait(&full[u % kStages], (u / kStages) & 1);
     }
     __syncwarp();
   } else {

@@ -18,7 +18,8 @@ struct DecodeKernelInfo {
 };
 
 bool decode_supported(int head_dim, int group);
-cudaError_t decode_kernel_info(int dtype, int head_dim, int group, int device, DecodeKernelInfo* info);
+cudaError_t decode_kernel_info(int dtype, int head_dim, int group, int device, DecodeKernelInfo* info,
+                               bool rope = false);
 cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int group, cudaStream_t stream);
 // Scratch bytes of one decode call with `splits` splits in clusters of
 // `cluster`: none when one cluster serves a group; otherwise a fixed region
@@ -37,5 +38,12 @@ cudaError_t launch_decode_bf16(const DecodeParams& p, int head_dim, int group, c
                                const cudaLaunchAttribute* attr);
 cudaError_t decode_info_f16(int head_dim, int group, DecodeKernelInfo* info);
 cudaError_t decode_info_bf16(int head_dim, int group, DecodeKernelInfo* info);
+// The same for the instances of the fused step with rotary embedding.
+cudaError_t launch_decode_f16_rope(const DecodeParams& p, int head_dim, int group, cudaStream_t stream,
+                                   const cudaLaunchAttribute* attr);
+cudaError_t launch_decode_bf16_rope(const DecodeParams& p, int head_dim, int group, cudaStream_t stream,
+                                    const cudaLaunchAttribute* attr);
+cudaError_t decode_info_f16_rope(int head_dim, int group, DecodeKernelInfo* info);
+cudaError_t decode_info_bf16_rope(int head_dim, int group, DecodeKernelInfo* info);
 
 }  // namespace da

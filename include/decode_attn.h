@@ -187,6 +187,28 @@ DA_API int decode_step_fwd(const void* q, void* k_cache, void* v_cache, const vo
                     void* workspace, size_t workspace_bytes, int max_kv_len_hint, int dtype,
                     int32_t* err_flag, void* stream);
 
+/*
+ * decode_step_fwd with the rotary position embedding the patched
+ * forward_step applies to the query and the new key before the append
+ * (VoxCPM issue #395, section 4.1: apply_rotary_pos_emb(query_states,
+ * key_states, cos, sin), then the write at position_id and the attention).
+ * q and k_new are the vectors before rotation; for sequence b with
+ * p = position_ids[b], every query head and the new key row become
+ *   x * cos[p] + rotate_half(x) * sin[p],  rotate_half(x) = [-x[D/2:], x[:D/2]]
+ * with each product and the sum rounded to fp32 (no fused multiply-add) and
+ * the result rounded to nearest even in the storage type; the rotated key row
+ * is what the cache receives. v_new is appended unchanged.
+ *   rope_cos, rope_sin  device fp32 tables [rope_rows, head_dim], row p
+ *                       holding the embedding of position p; 16-byte
+ *                       aligned; rope_rows >= capacity (else DA_ERR_SHAPE)
+ * Everything else as decode_step_fwd. NULL tables give DA_ERR_NULL.
+ */
+DA_API int decode_step_rope_fwd(const void* q, void* k_cache, void* v_cache, const void* k_new,
+                    const void* v_new, const float* rope_cos, const float* rope_sin, int rope_rows,
+                    const int32_t* position_ids, int B, int n_head, int n_kv_head, int head_dim,
+                    int capacity, float scale, void* out, void* workspace, size_t workspace_bytes,
+                    int max_kv_len_hint, int dtype, int32_t* err_flag, void* stream);
+
 /* Size of the library-owned scratch array used by
  * decode_attn_fwd_static_scratch (1 MiB per GPU that loads the library). */
 #define DA_STATIC_SCRATCH_BYTES (1u << 20)

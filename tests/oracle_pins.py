@@ -341,7 +341,10 @@ def pin_invalid_kv_len_gives_nan_rows(ora):
     sequence's rows are NaN and the other sequences are unaffected."""
     B, H, Hkv, D, cap, dtype = 3, 2, 1, 8, 6, "f16"
     q, k, v, _ = _case(B, H, Hkv, D, cap, dtype, [6, 6, 6], seed=4, finite_tail=True)
-    got = ora.decode_attn(_bits(q), _bits(k), _bits(v), np.array([0, 4, 7], np.int32), H, Hkv, dtype)
+    # The over-long length sits on the first sequence, so that an oracle
+    # that failed to reject it would read the next sequence's finite rows
+    # (defined memory) and give finite values instead of NaN.
+    got = ora.decode_attn(_bits(q), _bits(k), _bits(v), np.array([7, 4, 0], np.int32), H, Hkv, dtype)
     if not (np.all(np.isnan(got[0])) and np.all(np.isnan(got[2]))):
         raise AssertionError("invalid kv_len rows must be NaN")
     ref = _sdpa_prefix(q[1:2], k[1:2], v[1:2], np.array([4]), 1.0 / math.sqrt(D))

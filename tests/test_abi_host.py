@@ -135,6 +135,18 @@ def test_decode_step_and_append_reject_bad_arguments(lib):
     assert lib.kvcache_append(None, None, None, None, None, 0, 8, 128, 1024, 1, None, None) == 0
 
 
+def test_decode_step_rope_rejects_bad_tables(lib):
+    def rope(cos=A, sin=A, rows=1024, cap=1024):
+        return lib.decode_step_rope_fwd(A, A, A, A, A, cos, sin, rows, A, 1, 32, 8, 128, cap, 0.1, A, A, 1 << 30, 0, 1,
+                                        None, None)
+
+    assert rope(cos=None) == -1
+    assert rope(sin=None) == -1
+    assert rope(rows=1023) == -2          # every valid position needs a table row
+    assert rope(cos=A + 4) == -6
+    assert rope(sin=A + 8) == -6
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
 def test_valid_call_without_gpu_reports_cuda_error(lib):
     assert _fwd(lib) == -5
