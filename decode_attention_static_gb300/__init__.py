@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     STATIC_SCRATCH_BYTES,
     decode_attn_workspace_size,
     decode_step_fwd,
+    decode_step_layers_fwd,
     decode_step_rope_fwd,
     exported_symbols,
     kvcache_append,

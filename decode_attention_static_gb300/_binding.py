@@ -54,6 +54,8 @@ _SIGNATURES = {
                                         _vp], _i),
     "decode_step_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _vp, ctypes.c_size_t,
                          _i, _i, _vp, _vp], _i),
+    "decode_step_layers_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _vp,
+                                ctypes.c_size_t, _i, _i, _vp, _vp], _i),
     "decode_step_rope_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _vp,
                               ctypes.c_size_t, _i, _i, _vp, _vp], _i),
 }
@@ -264,6 +266,39 @@ def decode_step_rope_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.
                                              workspace.numel(), int(max_kv_len_hint), _dtype_code(q),
                                              _ptr(err_flag), _stream(q))
     _check("decode_step_rope_fwd", st)
+    return out
+
+
+def decode_step_layers_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, k_new: torch.Tensor,
+                           v_new: torch.Tensor, position_ids: torch.Tensor, out: torch.Tensor | None = None,
+                           scale: float | None = None, workspace: torch.Tensor | None = None,
+                           max_kv_len_hint: int = 0, err_flag: torch.Tensor | None = None) -> torch.Tensor:
+    """decode_step_fwd for every layer of [layers, ...]-stacked inputs and
+    caches in one call (layer l uses q[l], k_cache[l], ..., writes out[l])."""
+    if out is None:
+        out = torch.empty_like(q)
+    _require(q.dim() == 4 and k_cache.dim() == 5, "q must be [layers, B, H, D] and caches [layers, B, Hkv, cap, D]")
+    layers = q.shape[0]
+    if layers == 0:
+        return out
+    _require(k_cache.shape[0] == layers and v_cache.shape == k_cache.shape and out.shape == q.shape,
+             "every tensor needs the same leading layer count")
+    B, H, Hkv, D, cap = _attn_shapes(q[0], k_cache[0], v_cache[0], out[0])
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("out", out), ("k_new", k_new),
+                 ("v_new", v_new), ("position_ids", position_ids)):
+        _cuda_contig(n, t)
+    _require(tuple(k_new.shape) == (layers, B, Hkv, D) and v_new.shape == k_new.shape,
+             "k_new/v_new must be [layers, B, n_kv_head, D]")
+    _require(position_ids.dtype == torch.int32 and position_ids.numel() == B, "position_ids must be int32 [B]")
+    if scale is None:
+        scale = D ** -0.5
+    if workspace is None:
+        workspace = alloc_workspace(B, H, Hkv, D, cap, q.device)
+    st = load_library().decode_step_layers_fwd(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
+                                               _ptr(position_ids), layers, B, H, Hkv, D, cap, float(scale),
+                                               _ptr(out), _ptr(workspace), workspace.numel(), int(max_kv_len_hint),
+                                               _dtype_code(q), _ptr(err_flag), _stream(q))
+    _check("decode_step_layers_fwd", st)
     return out
 
 

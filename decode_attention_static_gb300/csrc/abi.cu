@@ -386,4 +386,30 @@ int decode_step_rope_fwd(const void* q, void* k_cache, void* v_cache, const void
                            dtype, err_flag, stream, rope_cos, rope_sin, rope_rows);
 }
 
+int decode_step_layers_fwd(const void* q, void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                           const int32_t* position_ids, int layers, int B, int n_head, int n_kv_head, int head_dim,
+                           int capacity, float scale, void* out, void* workspace, size_t workspace_bytes,
+                           int max_kv_len_hint, int dtype, int32_t* err_flag, void* stream) {
+  if (layers < 0) return DA_ERR_SHAPE;
+  if (layers == 0 || B == 0) return DA_OK;
+  int rc = da::check_sizes(B, n_head, n_kv_head, head_dim, capacity, dtype);
+  if (rc != DA_OK) return rc;
+  const size_t es = 2;  // bytes per element of both storage types
+  const size_t q_stride = (size_t)B * n_head * head_dim * es;
+  const size_t cache_stride = (size_t)B * n_kv_head * capacity * head_dim * es;
+  const size_t new_stride = (size_t)B * n_kv_head * head_dim * es;
+  for (int l = 0; l < layers; ++l) {
+    const size_t lq = (size_t)l * q_stride, lc = (size_t)l * cache_stride, ln = (size_t)l * new_stride;
+    auto at = [](const void* base, size_t off) -> const uint8_t* {
+      return base ? static_cast<const uint8_t*>(base) + off : nullptr;
+    };
+    auto at_w = [](void* base, size_t off) -> uint8_t* { return base ? static_cast<uint8_t*>(base) + off : nullptr; };
+    rc = da::decode_common(at(q, lq), at(k_cache, lc), at(v_cache, lc), at_w(k_cache, lc), at_w(v_cache, lc),
+                           at(k_new, ln), at(v_new, ln), position_ids, 1, B, n_head, n_kv_head, head_dim, capacity,
+                           scale, at_w(out, lq), workspace, workspace_bytes, max_kv_len_hint, dtype, err_flag, stream);
+    if (rc != DA_OK) return rc;
+  }
+  return DA_OK;
+}
+
 }  // extern "C"

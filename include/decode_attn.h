@@ -209,6 +209,29 @@ DA_API int decode_step_rope_fwd(const void* q, void* k_cache, void* v_cache, con
                     int capacity, float scale, void* out, void* workspace, size_t workspace_bytes,
                     int max_kv_len_hint, int dtype, int32_t* err_flag, void* stream);
 
+/*
+ * decode_step_fwd for `layers` layers of one model in one call: layer l
+ * reads q[l], k_new[l], v_new[l] and appends to and attends over its own
+ * caches k_cache[l], v_cache[l], writing out[l]:
+ *   q, out          [layers, B, n_head, head_dim]
+ *   k_cache, v_cache [layers, B, n_kv_head, capacity, head_dim]
+ *   k_new, v_new    [layers, B, n_kv_head, head_dim]
+ * all contiguous; position_ids [B] (the same step for every layer). The
+ * layers are launched in order on `stream`, each allowed to start its
+ * prologue while the previous one drains (programmatic dependent launch);
+ * they share the workspace, which is safe because each launch merges before
+ * the next one touches it. For a caller that holds every layer's inputs at
+ * once (benchmarks, replays captured in one CUDA graph). Validation as
+ * decode_step_fwd; every layer has the same sizes and (strides being
+ * multiples of 16 bytes) the same alignment, so an invalid argument is
+ * reported before the first launch. layers < 0 gives DA_ERR_SHAPE,
+ * layers == 0 does nothing.
+ */
+DA_API int decode_step_layers_fwd(const void* q, void* k_cache, void* v_cache, const void* k_new,
+                    const void* v_new, const int32_t* position_ids, int layers, int B, int n_head,
+                    int n_kv_head, int head_dim, int capacity, float scale, void* out, void* workspace,
+                    size_t workspace_bytes, int max_kv_len_hint, int dtype, int32_t* err_flag, void* stream);
+
 /* Size of the library-owned scratch array used by
  * decode_attn_fwd_static_scratch (1 MiB per GPU that loads the library). */
 #define DA_STATIC_SCRATCH_BYTES (1u << 20)

@@ -135,6 +135,17 @@ def test_decode_step_and_append_reject_bad_arguments(lib):
     assert lib.kvcache_append(None, None, None, None, None, 0, 8, 128, 1024, 1, None, None) == 0
 
 
+def test_decode_step_layers_rejects_bad_arguments(lib):
+    def layers_call(layers=2, k_new=A, D=128):
+        return lib.decode_step_layers_fwd(A, A, A, k_new, A, A, layers, 1, 32, 8, D, 1024, 0.1, A, A, 1 << 30, 0, 1,
+                                          None, None)
+
+    assert layers_call(layers=-1) == -2
+    assert layers_call(layers=0) == 0
+    assert layers_call(k_new=None) == -1
+    assert layers_call(D=96) == -3
+
+
 def test_decode_step_rope_rejects_bad_tables(lib):
     def rope(cos=A, sin=A, rows=1024, cap=1024):
         return lib.decode_step_rope_fwd(A, A, A, A, A, cos, sin, rows, A, 1, 32, 8, 128, cap, 0.1, A, A, 1 << 30, 0, 1,

@@ -270,3 +270,28 @@ def test_small_workspace_is_rejected():
         da.decode_attn_fwd(step.q, step.k_cache, step.v_cache, step.kv_len.contiguous(),
                            workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
     assert e.value.status == -4
+
+
+def test_layers_call_matches_per_layer_calls(ora):
+    """decode_step_layers_fwd over stacked layers gives, bit for bit, the
+    caches and outputs of one decode_step_fwd per layer, and the oracle's."""
+    layers, B, H, Hkv, D, cap, dt = 6, 2, 32, 8, 128, 1000, "bf16"
+    pos = [999, 400]
+    steps = [W.decode_step(B, H, Hkv, D, cap, dt, pos, seed=60 + l) for l in range(layers)]
+    stack = lambda name: torch.stack([getattr(s, name) for s in steps]).cuda()  # noqa: E731
+    q, kc, vc, kn, vn = (stack(n) for n in ("q", "k_cache", "v_cache", "k_new", "v_new"))
+    p = steps[0].position_ids.cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kc2, vc2 = kc.clone(), vc.clone()
+    out = da.decode_step_layers_fwd(q, kc, vc, kn, vn, p, max_kv_len_hint=cap, err_flag=err)
+    ref = torch.stack([da.decode_step_fwd(q[l], kc2[l], vc2[l], kn[l], vn[l], p, max_kv_len_hint=cap)
+                       for l in range(layers)])
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert torch.equal(kc.view(torch.int16), kc2.view(torch.int16))
+    assert torch.equal(vc.view(torch.int16), vc2.view(torch.int16))
+    for l in (0, layers - 1):
+        kb, vb, o = oracle_step(ora, steps[l])
+        assert np.array_equal(bits(kc[l]), kb) and np.array_equal(bits(vc[l]), vb)
+        assert_close(out[l], o, f"layer {l}")
