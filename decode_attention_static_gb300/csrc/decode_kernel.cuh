@@ -429,12 +429,15 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
     *abort_flag = 0;
     fence_mbar_init();
     // Pull the first tiles this CTA will probably read into L2, with rows
-    // from the host's length bound (clamped to the cache).
+    // from the host's length bound (clamped to the cache): two tiles when one
+    // sequence gives each CTA a short chunk (every CTA's first tiles then land
+    // sooner, the rest streams behind them), else a ring's worth.
     const int lh = p.len_hint;
     const int ch = split_chunk(lh, p.splits, Shape::kTileRows);
     const int pr0 = s * ch;
     if (pr0 < lh) {
-      const int rows = min(min(ch, lh - pr0), kStages * Shape::kTileRows);
+      const int ahead = (p.B == 1 && ch <= 6 * Shape::kTileRows) ? min(2, kStages) : kStages;
+      const int rows = min(min(ch, lh - pr0), ahead * Shape::kTileRows);
       for (int t0 = 0; t0 < rows; t0 += Shape::kTileRows) {
         const int n = min(Shape::kTileRows, rows - t0);
         const int64_t off = (kv_row0 + pr0 + t0) * Shape::kRowBytes;
