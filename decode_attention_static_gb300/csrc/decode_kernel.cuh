@@ -84,7 +84,9 @@ struct DecodeShape {
 // 16-bit values. A 3-stage ring of 32 KiB stages (96 KiB) per CTA covers the
 // loaded HBM latency and leaves room for two CTAs per SM: thread-block
 // clusters of up to 13 CTAs then fit once per group for 16 groups, and the
-// next launch's CTAs can be resident while this one drains. Eight elements
+// next launch's CTAs can be resident while this one drains. G >= 4 needs too
+// many registers for two CTAs per SM anyway and takes a 4-stage ring (more
+// bytes in flight for its long flat splits; 6 stages measured slower). Eight elements
 // per lane (one 16-byte vector of a row) give each warp more independent rows
 // per tile than sixteen, and fewer registers for the G query slices.
 template <int D, int G>
@@ -92,7 +94,7 @@ struct DecodeConfig {
   static constexpr int kWarps = 8;
   static constexpr int kPerLane = 8;
   static constexpr bool kPackedK = false;
-  static constexpr int kStages = 3;
+  static constexpr int kStages = G >= 4 ? 4 : 3;
 };
 
 // Merge the per-warp (m, l, acc) states kept in shared memory for head g,
