@@ -30,6 +30,7 @@ from ._binding import (  # noqa: F401
     set_timing_events,
     splits_for,
     status_string,
+    test_skip_slot,
     workspace_init,
 )
 

@@ -54,6 +54,7 @@ _SIGNATURES = {
                                         _vp], _i),
     "decode_step_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _vp, ctypes.c_size_t,
                          _i, _i, _vp, _vp], _i),
+    "da_test_skip_slot": ([_i], _i),
     "decode_step_layers_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _vp,
                                 ctypes.c_size_t, _i, _i, _vp, _vp], _i),
     "decode_step_rope_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _vp,
@@ -300,6 +301,13 @@ def decode_step_layers_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                                                _dtype_code(q), _ptr(err_flag), _stream(q))
     _check("decode_step_layers_fwd", st)
     return out
+
+
+def test_skip_slot(slot: int) -> None:
+    """Failure-detection test hook: with slot >= 0, later decode calls of this
+    thread leave that ring slot of one CTA unfilled, so its bounded waits
+    expire and the call reports DA_DEVERR_TIMEOUT (-1 turns it off)."""
+    load_library().da_test_skip_slot(int(slot))
 
 
 STATIC_SCRATCH_BYTES = 1 << 20  # DA_STATIC_SCRATCH_BYTES of the C header

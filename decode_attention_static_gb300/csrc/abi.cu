@@ -113,6 +113,8 @@ namespace {
 // Profiling hook events of this host thread (see da_set_timing_events).
 thread_local cudaEvent_t t_event_before = nullptr;
 thread_local cudaEvent_t t_event_after = nullptr;
+// Failure-detection test hook (da_test_skip_slot) of this host thread.
+thread_local int t_skip_slot = -1;
 
 cudaError_t record_event(cudaEvent_t ev, cudaStream_t st) {
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -205,6 +207,7 @@ int decode_common(const void* q, const void* k_cache, const void* v_cache, void*
   p.rope_sin = rope_sin;
   p.rope_rows = rope_rows;
   p.len_hint = bound;
+  p.skip_slot = t_skip_slot;
   // One sequence with an explicit bound: the bound is normally its length,
   // so the kernel issues its first tiles before reading the length.
   p.speculate = (B == 1 && max_kv_len_hint > 0) ? 1 : 0;
@@ -335,6 +338,11 @@ int decode_attn_splits_for(int B, int n_head, int n_kv_head, int head_dim, int c
   }
   if (cluster_size) *cluster_size = cluster;
   return splits;
+}
+
+int da_test_skip_slot(int slot) {
+  da::t_skip_slot = slot < 0 ? -1 : slot;
+  return DA_OK;
 }
 
 int da_set_timing_events(void* event_before, void* event_after) {

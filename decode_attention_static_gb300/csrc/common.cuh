@@ -310,6 +310,7 @@ struct DecodeParams {
   const float* rope_sin;
   int rope_rows;
   int len_hint;            // host bound on the active lengths (<= capacity): L2 prefetch, early tiles
+  int skip_slot;           // test hook: ring slot left unfilled in one CTA (< 0: none)
   int speculate;           // 1: len_hint is expected to be the exact length (early tiles are issued)
   int cluster;             // CTAs per thread-block cluster along the split axis (divides splits)
   float qscale;            // softmax scale * log2(e)

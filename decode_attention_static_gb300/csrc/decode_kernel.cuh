@@ -460,6 +460,8 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
   // Ring slot u takes rows [tr0, tr0 + rows) of this CTA's K and V, the row
   // at Lx - 1 from k_new/v_new in the fused step (producer lane only).
   auto issue = [&](int u, int tr0, int rows, int Lx) {
+    // Test hook: leave one slot of one CTA unfilled (its waits then time out).
+    if (u == p.skip_slot && s == 0 && b == 0 && g_kv == 0) return;
     const int stage = u % kStages;
     const bool new_last = fused && (tr0 + rows == Lx);
     const int cached = new_last ? rows - 1 : rows;

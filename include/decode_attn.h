@@ -145,6 +145,17 @@ DA_API int decode_attn_splits_for(int B, int n_head, int n_kv_head, int head_dim
 DA_API int da_set_timing_events(void* event_before, void* event_after);
 
 /*
+ * Failure-detection test hook. With slot >= 0, every later decode call made
+ * by this host thread leaves ring slot `slot` of the first split of sequence
+ * 0, KV head 0 unfilled: that CTA's pipeline waits run into their time limit
+ * (about one second), the CTA publishes NaN and the call sets
+ * DA_DEVERR_TIMEOUT; nothing faults and the context stays usable. Zero the
+ * workspace afterwards (as after any DA_DEVERR_TIMEOUT). slot < 0 turns the
+ * hook off (the default). Returns DA_OK.
+ */
+DA_API int da_test_skip_slot(int slot);
+
+/*
  * In-place append: k_cache[b, g, position_ids[b], :] = k_new[b, g, :] and the
  * same for V, for every sequence b and KV head g, copied bit for bit.
  * (VoxCPM issue #395, section 4.1.) A position outside [0, capacity) skips
