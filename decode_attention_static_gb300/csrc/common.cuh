@@ -2,7 +2,7 @@
 //
 // Inline PTX wrappers for the mbarrier / bulk-copy (TMA) pipeline, the
 // programmatic-dependent-launch controls, fp16/bf16 <-> fp32 conversion and
-// the split geometry shared by the decode and combine kernels.
+// the split geometry of the decode kernel.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -294,7 +294,7 @@ __device__ __forceinline__ void load_f32x8(const float* table, int64_t row, int 
   out[7] = __uint_as_float(b.w);
 }
 
-// Parameters shared by the decode and combine kernels.
+// Parameters of one decode-kernel launch.
 struct DecodeParams {
   const uint8_t* q;        // [B, n_head, D]
   const uint8_t* k_cache;  // [B, n_kv_head, capacity, D]

@@ -15,7 +15,7 @@ using ConfiguredShape = DecodeShape<D, G, DecodeConfig<D, G>::kWarps, DecodeConf
 template <typename T, int D, int G, bool RP>
 constexpr auto configured_kernel() {
   return decode_split_kernel<T, D, G, DecodeConfig<D, G>::kWarps, DecodeConfig<D, G>::kPerLane,
-                             DecodeConfig<D, G>::kPackedK, DecodeConfig<D, G>::kStages, RP>;
+                             DecodeConfig<D, G>::kStages, RP>;
 }
 
 template <typename T, int D, int G, bool RP>

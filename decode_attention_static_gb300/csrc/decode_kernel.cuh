@@ -12,13 +12,15 @@
 // (cp.async.bulk, contiguous rows of the cache) into a kStages-deep ring of
 // shared-memory stages guarded by full/empty mbarriers. CW consumer warps
 // read the stages with 128-bit shared loads: a row of D elements is spread
-// over D/DPL lanes holding DPL elements each (one or two 16-byte vectors),
-// and each lane keeps its slice of the G query vectors in registers,
-// pre-multiplied by scale * log2(e). Scores are reduced across the lanes of a
-// row with xor shuffles; every group of lanes keeps an fp32 online-softmax
+// over D/8 lanes holding one 16-byte vector each, and each lane keeps its
+// slice of the G query vectors in registers (raw 16-bit; scores are scaled
+// by scale * log2(e) after the dot product). Scores are reduced across the
+// lanes of a row with xor shuffles; every group of lanes keeps an fp32 online-softmax
 // state (running max m, sum l, accumulator acc) in the base-2 domain (the
 // max-subtracted fp32 softmax of Cuda-Compute-OSS issue #343, "Proposed
-// implementation").
+// implementation"). The fused step reads the attended row L - 1 from k_new
+// and v_new and writes it into the cache; with rotary embedding (RP) q and
+// that key row are rotated first (VoxCPM issue #395, section 4.1).
 //
 // Merge of the splits. The splits of one (b, g) group are launched as
 // thread-block clusters of `cluster` CTAs. Each CTA folds its warps' states
@@ -77,11 +79,9 @@ struct DecodeShape {
   static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
 };
 
-// Consumer warps, elements per lane, score arithmetic and ring depth of each
-// instance. kPackedK: convert each K element once and form the G dot
-// products with packed fp32x2 FMAs on fp32 q (fewer instructions when
-// G >= 4); otherwise one mixed-precision FMA per element and head on the raw
-// 16-bit values. A 3-stage ring of 32 KiB stages (96 KiB) per CTA covers the
+// Consumer warps, elements per lane and ring depth of each instance. Scores
+// take one mixed-precision FMA per element and head on the raw 16-bit q and
+// K (packed fp32x2 products on converted K measured no faster). A 3-stage ring of 32 KiB stages (96 KiB) per CTA covers the
 // loaded HBM latency and leaves room for two CTAs per SM: thread-block
 // clusters of up to 13 CTAs then fit once per group for 16 groups, and the
 // next launch's CTAs can be resident while this one drains. G >= 4 needs too
@@ -93,7 +93,6 @@ template <int D, int G>
 struct DecodeConfig {
   static constexpr int kWarps = 8;
   static constexpr int kPerLane = 8;
-  static constexpr bool kPackedK = false;
   static constexpr int kStages = G >= 4 ? 4 : 3;
 };
 
@@ -156,10 +155,9 @@ constexpr float kLazyRescale = 8.f;
 // weighted V accumulation (packed fp32x2 FMAs). `kt`/`vt` point at this lane
 // group's first row of the tile; with kFull false only rows whose offset
 // from it is below `left` (in lane-group steps) are valid.
-template <typename S, typename Shape, int G, bool kFull, bool kPacked>
+template <typename S, typename Shape, int G, bool kFull>
 __device__ __forceinline__ void consume_tile(const uint8_t* kt, const uint8_t* vt, int left,
-                                             const uint4 (&q)[G][Shape::kVecs],
-                                             const float2 (&qf)[kPacked ? G : 1][Shape::kVecs][4], float qscale,
+                                             const uint4 (&q)[G][Shape::kVecs], float qscale,
                                              int c, int swap, float (&m)[G], float& l_own,
                                              float2 (&acc)[G][Shape::kVecs][4]) {
   constexpr int NV = Shape::kVecs;
@@ -170,42 +168,23 @@ __device__ __forceinline__ void consume_tile(const uint8_t* kt, const uint8_t* v
   for (int u = 0; u < Shape::kSteps; ++u) {
     const bool valid = kFull || u * Shape::kRowsPerStep < left;
     float part[G];
-    if constexpr (kPacked) {
-      float2 a[G];
+    float a0[G], a1[G];
 #pragma unroll
-      for (int g = 0; g < G; ++g) a[g] = make_float2(0.f, 0.f);
+    for (int g = 0; g < G; ++g) a0[g] = a1[g] = 0.f;
 #pragma unroll
-      for (int j = 0; j < NV; ++j) {
-        uint4 kv = make_uint4(0u, 0u, 0u, 0u);
-        if (valid) kv = *reinterpret_cast<const uint4*>(kt + u * RS + (c + LPR * (j ^ swap)) * 16);
-        float2 kf[4];
-        S::unpack2(kv, kf);
+    for (int j = 0; j < NV; ++j) {
+      uint4 kv = make_uint4(0u, 0u, 0u, 0u);
+      if (valid) kv = *reinterpret_cast<const uint4*>(kt + u * RS + (c + LPR * (j ^ swap)) * 16);
 #pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) a[g] = __ffma2_rn(qf[g][j][e], kf[e], a[g]);
+      for (int g = 0; g < G; ++g) {
+        S::dot2(q[g][j].x, kv.x, a0[g], a1[g]);
+        S::dot2(q[g][j].y, kv.y, a0[g], a1[g]);
+        S::dot2(q[g][j].z, kv.z, a0[g], a1[g]);
+        S::dot2(q[g][j].w, kv.w, a0[g], a1[g]);
       }
-#pragma unroll
-      for (int g = 0; g < G; ++g) part[g] = a[g].x + a[g].y;
-    } else {
-      float a0[G], a1[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) a0[g] = a1[g] = 0.f;
-#pragma unroll
-      for (int j = 0; j < NV; ++j) {
-        uint4 kv = make_uint4(0u, 0u, 0u, 0u);
-        if (valid) kv = *reinterpret_cast<const uint4*>(kt + u * RS + (c + LPR * (j ^ swap)) * 16);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          S::dot2(q[g][j].x, kv.x, a0[g], a1[g]);
-          S::dot2(q[g][j].y, kv.y, a0[g], a1[g]);
-          S::dot2(q[g][j].z, kv.z, a0[g], a1[g]);
-          S::dot2(q[g][j].w, kv.w, a0[g], a1[g]);
-        }
-      }
-#pragma unroll
-      for (int g = 0; g < G; ++g) part[g] = a0[g] + a1[g];
     }
+#pragma unroll
+    for (int g = 0; g < G; ++g) part[g] = a0[g] + a1[g];
     // Sum over the LPR lanes of the row. With one head this is a butterfly.
     // With several, each halving step sends the half of the heads this lane
     // gives up and adds the partner's half of the ones it keeps; after
@@ -215,7 +194,7 @@ __device__ __forceinline__ void consume_tile(const uint8_t* kt, const uint8_t* v
       float v = part[0];
 #pragma unroll
       for (int off = LPR / 2; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      own[u] = valid ? (kPacked ? v : v * qscale) : -INFINITY;
+      own[u] = valid ? v * qscale : -INFINITY;
     } else {
 #pragma unroll
       for (int n = G, off = LPR / 2; n > 1; n >>= 1, off >>= 1) {
@@ -230,7 +209,7 @@ __device__ __forceinline__ void consume_tile(const uint8_t* kt, const uint8_t* v
       float v = part[0];
 #pragma unroll
       for (int off = LPR / (2 * G); off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      own[u] = valid ? (kPacked ? v : v * qscale) : -INFINITY;
+      own[u] = valid ? v * qscale : -INFINITY;
     }
   }
 
@@ -388,7 +367,7 @@ __device__ __forceinline__ void merge_partials(const DecodeParams& p, int64_t he
   }
 }
 
-template <typename T, int D, int G, int CW, int DPL, bool PK, int NS, bool RP>
+template <typename T, int D, int G, int CW, int DPL, int NS, bool RP>
 __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const DecodeParams p) {
   using Shape = DecodeShape<D, G, CW, DPL, NS>;
   constexpr int kStages = NS;
@@ -690,19 +669,6 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
         for (int e = 0; e < 4; ++e) acc[g][j][e] = make_float2(0.f, 0.f);
     }
     const int lane_off = (warp * Shape::kRowsPerWarp + lrow) * Shape::kRowBytes;
-    float2 qf[PK ? G : 1][NV][4];  // fp32 q pre-multiplied by the scale (packed path only)
-    if constexpr (PK) {
-#pragma unroll
-      for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int j = 0; j < NV; ++j) {
-          float2 f[4];
-          S::unpack2(qraw[g][j], f);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) qf[g][j][e] = make_float2(f[e].x * p.qscale, f[e].y * p.qscale);
-        }
-    }
-
     bool aborted = false;
     // Discarded early tiles: their copies must have landed (phase 0 of their
     // stages) before this warp waits on a later phase of the same stages; a
@@ -722,10 +688,10 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
       const uint8_t* vt = kt + kTileBytes;
       const int rows = min(Shape::kTileRows, r1 - (r0 + t * Shape::kTileRows));
       if (rows == Shape::kTileRows) {
-        consume_tile<S, Shape, G, true, PK>(kt, vt, 0, qraw, qf, p.qscale, c, swap, m, l_own, acc);
+        consume_tile<S, Shape, G, true>(kt, vt, 0, qraw, p.qscale, c, swap, m, l_own, acc);
       } else {
-        consume_tile<S, Shape, G, false, PK>(kt, vt, rows - (warp * Shape::kRowsPerWarp + lrow), qraw, qf,
-                                             p.qscale, c, swap, m, l_own, acc);
+        consume_tile<S, Shape, G, false>(kt, vt, rows - (warp * Shape::kRowsPerWarp + lrow), qraw, p.qscale, c,
+                                         swap, m, l_own, acc);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[stage]);
