@@ -59,14 +59,27 @@ def test_matches_workspace_entry_point_on_two_calls_in_a_row(ora):
 
 def test_rejects_sizes_beyond_the_scratch_limit():
     """A split plan needing more than the fixed array is refused before any
-    launch. The plan keeps all split CTAs in one wave, so on a 152-SM GPU no
-    supported shape needs more than about 0.95 MiB; the check is then only
-    reachable on GPUs with more resident CTAs, and the test skips."""
-    step = W.decode_step(2, 32, 8, 128, 32768, "bf16", [32767, 32767], seed=23)
-    splits, need = _scratch_need(step, 0)
+    launch (DA_ERR_SHAPE). Two sequences of a long cache with 8 query heads
+    per KV head give a flat plan of about 1.2 MiB of partials on a 152-SM
+    GPU; the first candidate shape whose plan exceeds the array is used."""
+    candidates = [W.decode_step(2, 64, 8, 128, 32768, "bf16", [32767, 30000], seed=23),
+                  W.decode_step(2, 32, 8, 128, 32768, "bf16", [32767, 32767], seed=24)]
+    for step in candidates:
+        splits, need = _scratch_need(step, 0)
+        if need > da.STATIC_SCRATCH_BYTES:
+            break
+    else:
+        pytest.skip(f"no candidate split plan exceeds the scratch array on this GPU (largest {need} B)")
     d = step.to("cuda")
-    if need <= da.STATIC_SCRATCH_BYTES:
-        pytest.skip(f"this GPU's largest split plan ({need} B) fits the scratch array")
     with pytest.raises(da.DecodeAttnError) as e:
         da.decode_attn_fwd_static_scratch(d.q, d.k_cache, d.v_cache, d.kv_len.contiguous())
     assert e.value.status == -2
+    # nothing was enqueued and the array is untouched: a fitting call still works
+    small = W.long_context(seed=25, kv_len=20000)
+    ds = small.to("cuda")
+    da.kvcache_append(ds.k_cache, ds.v_cache, ds.k_new, ds.v_new, ds.position_ids)
+    got = da.decode_attn_fwd_static_scratch(ds.q, ds.k_cache, ds.v_cache, ds.kv_len.contiguous())
+    ref = da.decode_attn_fwd(ds.q, ds.k_cache, ds.v_cache, ds.kv_len.contiguous())
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(got.float()).all())
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
