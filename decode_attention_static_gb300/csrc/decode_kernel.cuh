@@ -791,8 +791,9 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
   // pushes its (m, l) and, for each rank, the slice of its accumulator that
   // rank merges into that rank's receive area (distributed shared-memory
   // stores, no round trips); after one cluster barrier each CTA merges its
-  // slice from its own shared memory. Nothing is read remotely, so a CTA
-  // may leave as soon as it has merged.
+  // slice from its own shared memory, one output per 16 lanes (lane r holds
+  // rank r; the max and the sums are shuffle reductions). Nothing is read
+  // remotely, so a CTA may leave as soon as it has merged.
   const int per = (E + CS - 1) / CS;  // outputs merged by each CTA of the cluster
   const int e0 = rank * per;
   const int e1 = min(E, e0 + per);
@@ -811,31 +812,9 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
     cluster_arrive_release();
     cluster_wait_acquire();
   }
-  for (int i = e0 + (int)threadIdx.x; i < e1; i += Shape::kThreads) {
+  auto emit = [&](int i, float mm, float ls, float as) {
     const int g = i / D;
     const int d = i % D;
-    float mm, ls, as;
-    if (CS == 1) {
-      mm = state[E + g];
-      ls = state[E + G + g];
-      as = state[i];
-    } else {
-      mm = -INFINITY;
-#pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r)
-        if (r < CS) mm = fmaxf(mm, ml_in[r * 2 * G + g]);
-      ls = 0.f;
-      as = 0.f;
-#pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r) {
-        if (r < CS) {
-          const float mr = ml_in[r * 2 * G + g];
-          const float f = (mr == -INFINITY) ? 0.f : fast_exp2(mr - mm);
-          ls = fmaf(ml_in[r * 2 * G + G + g], f, ls);
-          as = fmaf(acc_in[r * per + (i - e0)], f, as);
-        }
-      }
-    }
     if (nclusters == 1) {
       store_out<T>(p, head0 * D + i, as / ls);
     } else {
@@ -845,6 +824,36 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
         p.ws_ml[base * 2] = mm;
         p.ws_ml[base * 2 + 1] = ls;
       }
+    }
+  };
+  if (CS == 1) {
+    for (int i = e0 + (int)threadIdx.x; i < e1; i += Shape::kThreads)
+      emit(i, state[E + i / D], state[E + G + i / D], state[i]);
+  } else {
+    // 16 lanes per output, lane r holding rank r: the max and the two sums
+    // are xor-shuffle reductions over those lanes (all loads independent).
+    static_assert(kMaxCluster <= 16, "16 lanes per output cover every rank of a cluster");
+    const int r = lane & 15;
+    const int n_out = e1 - e0;
+    for (int j0 = warp * 2; j0 < n_out; j0 += (Shape::kThreads / 32) * 2) {
+      const int j = j0 + (lane >> 4);
+      const bool ok = r < CS && j < n_out;
+      const int i = e0 + min(j, n_out - 1);
+      const int g = i / D;
+      const float mr = ok ? ml_in[r * 2 * G + g] : -INFINITY;
+      const float lr = ok ? ml_in[r * 2 * G + G + g] : 0.f;
+      const float ar = ok ? acc_in[r * per + (i - e0)] : 0.f;
+      float mm = mr;
+#pragma unroll
+      for (int off = 8; off >= 1; off >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, off));
+      const float w = (mr == -INFINITY) ? 0.f : fast_exp2(mr - mm);
+      float ls = lr * w, as = ar * w;
+#pragma unroll
+      for (int off = 8; off >= 1; off >>= 1) {
+        ls += __shfl_xor_sync(0xffffffffu, ls, off);
+        as += __shfl_xor_sync(0xffffffffu, as, off);
+      }
+      if (r == 0 && j < n_out) emit(i, mm, ls, as);
     }
   }
 
