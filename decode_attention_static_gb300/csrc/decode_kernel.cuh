@@ -791,9 +791,10 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
   // pushes its (m, l) and, for each rank, the slice of its accumulator that
   // rank merges into that rank's receive area (distributed shared-memory
   // stores, no round trips); after one cluster barrier each CTA merges its
-  // slice from its own shared memory, one output per 16 lanes (lane r holds
-  // rank r; the max and the sums are shuffle reductions). Nothing is read
-  // remotely, so a CTA may leave as soon as it has merged.
+  // slice from its own shared memory: a narrow slice one output per 16 lanes
+  // (lane r holds rank r; the max and the sums are shuffle reductions), a
+  // wide one one output per thread. Nothing is read remotely, so a CTA may
+  // leave as soon as it has merged.
   const int per = (E + CS - 1) / CS;  // outputs merged by each CTA of the cluster
   const int e0 = rank * per;
   const int e1 = min(E, e0 + per);
@@ -826,16 +827,38 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
       }
     }
   };
+  constexpr int kLaneOutputs = 2 * (Shape::kThreads / 32);  // outputs per pass of the 16-lane merge
   if (CS == 1) {
     for (int i = e0 + (int)threadIdx.x; i < e1; i += Shape::kThreads)
       emit(i, state[E + i / D], state[E + G + i / D], state[i]);
+  } else if (e1 - e0 > 2 * kLaneOutputs) {
+    // A wide slice over few ranks: one thread per output, ranks in turn.
+    for (int i = e0 + (int)threadIdx.x; i < e1; i += Shape::kThreads) {
+      const int g = i / D;
+      float mm = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r)
+        if (r < CS) mm = fmaxf(mm, ml_in[r * 2 * G + g]);
+      float ls = 0.f, as = 0.f;
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r) {
+        if (r < CS) {
+          const float mr = ml_in[r * 2 * G + g];
+          const float f = (mr == -INFINITY) ? 0.f : fast_exp2(mr - mm);
+          ls = fmaf(ml_in[r * 2 * G + G + g], f, ls);
+          as = fmaf(acc_in[r * per + (i - e0)], f, as);
+        }
+      }
+      emit(i, mm, ls, as);
+    }
   } else {
-    // 16 lanes per output, lane r holding rank r: the max and the two sums
-    // are xor-shuffle reductions over those lanes (all loads independent).
+    // A narrow slice (at most two passes): 16 lanes per output, lane r
+    // holding rank r; the max and the two sums are xor-shuffle reductions
+    // over those lanes (all loads independent).
     static_assert(kMaxCluster <= 16, "16 lanes per output cover every rank of a cluster");
     const int r = lane & 15;
     const int n_out = e1 - e0;
-    for (int j0 = warp * 2; j0 < n_out; j0 += (Shape::kThreads / 32) * 2) {
+    for (int j0 = warp * 2; j0 < n_out; j0 += kLaneOutputs) {
       const int j = j0 + (lane >> 4);
       const bool ok = r < CS && j < n_out;
       const int i = e0 + min(j, n_out - 1);
