@@ -478,6 +478,7 @@ def run_ours(args) -> dict | None:
         "clocks": clk,
     }
     if not args.no_extras and rank == 0:
+        out["attend_only"] = attend_only(torch, da, device, step.l2_bytes)
         out["kv_curve"] = kv_curve(torch, da, device, step.l2_bytes)
         out["configs"] = other_configs(torch, da, device, step.l2_bytes)
     if not args.no_cpu_baseline:
@@ -554,6 +555,32 @@ def kv_curve(torch, da, device, l2_bytes: int) -> list:
         s, cs = da.splits_for(1, H, Hkv, D, kv, kv, dt)
         res.append({"kv_len": kv, "layers": layers, "splits": s, "cluster": cs, "us_per_layer_step": round(us, 3),
                     "gbs": round(b / (us * 1e-6) / 1e9, 1)})
+        del k, v
+    return res
+
+
+def attend_only(torch, da, device, l2_bytes: int) -> list:
+    """The sweep's shape (B=1, 16/16 heads, head_dim 128, fp16) with attention
+    alone (decode_attn_fwd on a prefix already in the cache, no append), over
+    rotating layer caches totalling at least 3x L2: the step without its
+    append."""
+    res = []
+    for kv in SWEEP:
+        layers = layers_for(kv, l2_bytes)
+        k = torch.empty(layers, B, N_KV_HEAD, kv, HEAD_DIM, dtype=torch.float16, device=device).normal_()
+        v = torch.empty_like(k).normal_()
+        q = torch.empty(layers, B, N_HEAD, HEAD_DIM, dtype=torch.float16, device=device).normal_()
+        out = torch.empty_like(q)
+        lens = torch.full((B,), kv, dtype=torch.int32, device=device)
+        ws = da.alloc_workspace(B, N_HEAD, N_KV_HEAD, HEAD_DIM, kv)
+
+        def issue():
+            for l in range(layers):
+                da.decode_attn_fwd(q[l], k[l], v[l], lens, out=out[l], workspace=ws, max_kv_len_hint=kv)
+
+        us = graph_us_per_call(torch, device, issue, layers, reps=max(3, 2000 // layers))
+        b = attend_bytes(B, N_HEAD, N_KV_HEAD, HEAD_DIM, [kv])
+        res.append({"kv_len": kv, "us_per_call": round(us, 3), "gbs": round(b / (us * 1e-6) / 1e9, 1)})
         del k, v
     return res
 
