@@ -175,3 +175,25 @@ def test_binding_checks_tensor_arguments():
     with pytest.raises(ValueError):
         da.decode_attn_fwd(cpu, torch.zeros(1, 1, 8, 64, dtype=torch.float16),
                            torch.zeros(1, 1, 8, 64, dtype=torch.float16), torch.ones(1, dtype=torch.int32))
+
+
+def test_plain_c_program_uses_the_library(lib, tmp_path):
+    """The boundary is a C ABI: the header compiles as C99, and a plain C
+    program links against the library and calls host-only entry points."""
+    src = tmp_path / "consumer.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <string.h>\n#include "decode_attn.h"\n'
+        "int main(void) {\n"
+        "  int cs = 0;\n"
+        "  int s = decode_attn_plan_splits(1, 16, 128, 8192, 152, 2, 16, &cs);\n"
+        '  if (da_version() <= 0 || strcmp(da_status_string(DA_OK), "") == 0) return 1;\n'
+        "  if (decode_attn_plan_splits(0, 16, 128, 8192, 152, 2, 16, &cs) != DA_ERR_SHAPE) return 2;\n"
+        '  printf("%d %d\\n", s, cs);\n'
+        "  return s >= 1 && cs >= 1 ? 0 : 3;\n}\n")
+    exe = tmp_path / "consumer"
+    libdir = da.library_path().parent
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-pedantic", str(src), f"-I{ROOT / 'include'}",
+                    f"-L{libdir}", f"-l:{da.library_path().name}", f"-Wl,-rpath,{libdir}", "-o", str(exe)],
+                   check=True, capture_output=True, text=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    assert (int(out[0]), int(out[1])) == da.plan_splits(1, 16, 128, 8192, 152, 2)
