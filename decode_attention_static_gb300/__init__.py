@@ -27,6 +27,8 @@ from ._binding import (  # noqa: F401
     library_path,
     load_library,
     plan_splits,
+    prefix_ready,
+    set_prefix_ready,
     set_timing_events,
     splits_for,
     status_string,

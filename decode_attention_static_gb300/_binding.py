@@ -8,6 +8,7 @@ library's kernels. If the library has not been built, every call raises
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import pathlib
 
@@ -55,6 +56,7 @@ _SIGNATURES = {
     "decode_step_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _vp, ctypes.c_size_t,
                          _i, _i, _vp, _vp], _i),
     "da_test_skip_slot": ([_i], _i),
+    "da_set_prefix_ready": ([_i], _i),
     "decode_step_layers_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _vp,
                                 ctypes.c_size_t, _i, _i, _vp, _vp], _i),
     "decode_step_rope_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _vp,
@@ -102,10 +104,14 @@ def _stream(t: torch.Tensor) -> ctypes.c_void_p:
     return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
 
 
+def _code_for(dtype: torch.dtype) -> int:
+    if dtype not in _DTYPE_CODE:
+        raise TypeError(f"dtype {dtype} is not supported (float16 or bfloat16)")
+    return _DTYPE_CODE[dtype]
+
+
 def _dtype_code(t: torch.Tensor) -> int:
-    if t.dtype not in _DTYPE_CODE:
-        raise TypeError(f"dtype {t.dtype} is not supported (float16 or bfloat16)")
-    return _DTYPE_CODE[t.dtype]
+    return _code_for(t.dtype)
 
 
 def _require(cond: bool, msg: str) -> None:
@@ -116,6 +122,35 @@ def _require(cond: bool, msg: str) -> None:
 def _cuda_contig(name: str, t: torch.Tensor) -> None:
     _require(t.is_cuda, f"{name} must be a CUDA tensor")
     _require(t.is_contiguous(), f"{name} must be contiguous")
+
+
+def _on(device: torch.device, **tensors: torch.Tensor) -> None:
+    """Every named tensor is a contiguous CUDA tensor on `device`."""
+    for name, t in tensors.items():
+        _cuda_contig(name, t)
+        _require(t.device == device, f"{name} is on {t.device}, the inputs on {device}")
+
+
+def _err_ptr(err_flag: torch.Tensor | None, device: torch.device):
+    if err_flag is None:
+        return None
+    _on(device, err_flag=err_flag)
+    _require(err_flag.dtype == torch.int32 and err_flag.numel() >= 1, "err_flag must be int32 with one element")
+    return _ptr(err_flag)
+
+
+def _workspace(workspace: torch.Tensor, device: torch.device):
+    """(pointer, size in bytes) of a caller workspace."""
+    _on(device, workspace=workspace)
+    return _ptr(workspace), workspace.numel() * workspace.element_size()
+
+
+def _call(fn: str, device: torch.device, *args) -> None:
+    """Call entry point `fn` with `device` current (the library launches on
+    the current device, on the stream passed in `args`)."""
+    with torch.cuda.device(device):
+        st = getattr(load_library(), fn)(*args)
+    _check(fn, st)
 
 
 def plan_splits(B: int, n_kv_head: int, head_dim: int, max_kv_len: int, num_sms: int, ctas_per_sm: int,
@@ -143,9 +178,8 @@ def alloc_workspace(B: int, n_head: int, n_kv_head: int, head_dim: int, capacity
 
 def workspace_init(workspace: torch.Tensor) -> None:
     """Zero-fill a workspace on the current stream (needed once before first use)."""
-    _cuda_contig("workspace", workspace)
-    st = load_library().decode_attn_workspace_init(_ptr(workspace), workspace.numel(), _stream(workspace))
-    _check("decode_attn_workspace_init", st)
+    ws, ws_bytes = _workspace(workspace, workspace.device)
+    _call("decode_attn_workspace_init", workspace.device, ws, ws_bytes, _stream(workspace))
 
 
 def splits_for(B: int, n_head: int, n_kv_head: int, head_dim: int, capacity: int, max_kv_len_hint: int = 0,
@@ -153,7 +187,7 @@ def splits_for(B: int, n_head: int, n_kv_head: int, head_dim: int, capacity: int
     """(splits, cluster size) decode_attn_fwd will use for these sizes on the current device."""
     cs = ctypes.c_int(0)
     s = load_library().decode_attn_splits_for(B, n_head, n_kv_head, head_dim, capacity, int(max_kv_len_hint),
-                                              _DTYPE_CODE[dtype], ctypes.byref(cs))
+                                              _code_for(dtype), ctypes.byref(cs))
     _check("decode_attn_splits_for", s if s < 0 else 0)
     return s, cs.value
 
@@ -170,22 +204,21 @@ def set_timing_events(before: "torch.cuda.Event | None", after: "torch.cuda.Even
 def kvcache_append(k_cache: torch.Tensor, v_cache: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                    position_ids: torch.Tensor, err_flag: torch.Tensor | None = None) -> None:
     """k_cache[b, g, position_ids[b]] = k_new[b, g] (and V), in place."""
-    for n, t in (("k_cache", k_cache), ("v_cache", v_cache), ("k_new", k_new), ("v_new", v_new),
-                 ("position_ids", position_ids)):
-        _cuda_contig(n, t)
+    _cuda_contig("k_cache", k_cache)
+    dev = k_cache.device
+    _on(dev, v_cache=v_cache, k_new=k_new, v_new=v_new, position_ids=position_ids)
     _require(k_cache.dim() == 4 and v_cache.shape == k_cache.shape, "caches must be [B, n_kv_head, capacity, D]")
     B, Hkv, cap, D = k_cache.shape
     _require(tuple(k_new.shape) == (B, Hkv, D) and v_new.shape == k_new.shape, "k_new/v_new must be [B, n_kv_head, D]")
     _require(position_ids.dtype == torch.int32 and position_ids.numel() == B, "position_ids must be int32 [B]")
     _require(k_new.dtype == k_cache.dtype == v_cache.dtype == v_new.dtype, "dtypes differ")
-    st = load_library().kvcache_append(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(position_ids),
-                                       B, Hkv, D, cap, _dtype_code(k_cache), _ptr(err_flag), _stream(k_cache))
-    _check("kvcache_append", st)
+    _call("kvcache_append", dev, _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(position_ids), B, Hkv,
+          D, cap, _dtype_code(k_cache), _err_ptr(err_flag, dev), _stream(k_cache))
 
 
 def _attn_shapes(q, k_cache, v_cache, out):
-    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("out", out)):
-        _cuda_contig(n, t)
+    _cuda_contig("q", q)
+    _on(q.device, k_cache=k_cache, v_cache=v_cache, out=out)
     _require(q.dim() == 3, "q must be [B, n_head, D]")
     _require(k_cache.dim() == 4 and v_cache.shape == k_cache.shape, "caches must be [B, n_kv_head, capacity, D]")
     B, H, D = q.shape
@@ -203,17 +236,32 @@ def decode_attn_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
     if out is None:
         out = torch.empty_like(q)
     B, H, Hkv, D, cap = _attn_shapes(q, k_cache, v_cache, out)
-    _cuda_contig("kv_len", kv_len)
+    dev = q.device
+    _on(dev, kv_len=kv_len)
     _require(kv_len.dtype == torch.int32 and kv_len.numel() == B, "kv_len must be int32 [B]")
     if scale is None:
         scale = D ** -0.5
     if workspace is None:
-        workspace = alloc_workspace(B, H, Hkv, D, cap, q.device)
-    st = load_library().decode_attn_fwd(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), B, H, Hkv, D, cap,
-                                        float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
-                                        int(max_kv_len_hint), _dtype_code(q), _ptr(err_flag), _stream(q))
-    _check("decode_attn_fwd", st)
+        workspace = alloc_workspace(B, H, Hkv, D, cap, dev)
+    ws, ws_bytes = _workspace(workspace, dev)
+    _call("decode_attn_fwd", dev, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), B, H, Hkv, D, cap,
+          float(scale), _ptr(out), ws, ws_bytes, int(max_kv_len_hint), _dtype_code(q), _err_ptr(err_flag, dev),
+          _stream(q))
     return out
+
+
+def _step_inputs(q, k_cache, v_cache, k_new, v_new, position_ids, out, lead=()):
+    """Shapes of a fused step: q [*lead, B, H, D], caches [*lead, B, Hkv, cap, D],
+    k_new/v_new [*lead, B, Hkv, D], position_ids int32 [B]."""
+    n = len(lead)
+    B, H, Hkv, D, cap = _attn_shapes(q[(0,) * n], k_cache[(0,) * n], v_cache[(0,) * n], out[(0,) * n])
+    _on(q.device, q=q, k_cache=k_cache, v_cache=v_cache, out=out, k_new=k_new, v_new=v_new,
+        position_ids=position_ids)
+    _require(tuple(k_new.shape) == (*lead, B, Hkv, D) and v_new.shape == k_new.shape,
+             "k_new/v_new must be [" + "layers, " * n + "B, n_kv_head, D]")
+    _require(k_new.dtype == v_new.dtype == q.dtype, "dtypes differ")
+    _require(position_ids.dtype == torch.int32 and position_ids.numel() == B, "position_ids must be int32 [B]")
+    return B, H, Hkv, D, cap
 
 
 def decode_step_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, k_new: torch.Tensor,
@@ -223,20 +271,16 @@ def decode_step_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
     """Fused append at position_ids then attention over [0, position_ids]."""
     if out is None:
         out = torch.empty_like(q)
-    B, H, Hkv, D, cap = _attn_shapes(q, k_cache, v_cache, out)
-    for n, t in (("k_new", k_new), ("v_new", v_new), ("position_ids", position_ids)):
-        _cuda_contig(n, t)
-    _require(tuple(k_new.shape) == (B, Hkv, D) and v_new.shape == k_new.shape, "k_new/v_new must be [B, n_kv_head, D]")
-    _require(position_ids.dtype == torch.int32 and position_ids.numel() == B, "position_ids must be int32 [B]")
+    B, H, Hkv, D, cap = _step_inputs(q, k_cache, v_cache, k_new, v_new, position_ids, out)
+    dev = q.device
     if scale is None:
         scale = D ** -0.5
     if workspace is None:
-        workspace = alloc_workspace(B, H, Hkv, D, cap, q.device)
-    st = load_library().decode_step_fwd(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
-                                        _ptr(position_ids), B, H, Hkv, D, cap, float(scale), _ptr(out),
-                                        _ptr(workspace), workspace.numel(), int(max_kv_len_hint), _dtype_code(q),
-                                        _ptr(err_flag), _stream(q))
-    _check("decode_step_fwd", st)
+        workspace = alloc_workspace(B, H, Hkv, D, cap, dev)
+    ws, ws_bytes = _workspace(workspace, dev)
+    _call("decode_step_fwd", dev, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
+          _ptr(position_ids), B, H, Hkv, D, cap, float(scale), _ptr(out), ws, ws_bytes, int(max_kv_len_hint),
+          _dtype_code(q), _err_ptr(err_flag, dev), _stream(q))
     return out
 
 
@@ -249,24 +293,19 @@ def decode_step_rope_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.
     position_ids (tables rope_cos/rope_sin fp32 [rows, D], rows >= capacity)."""
     if out is None:
         out = torch.empty_like(q)
-    B, H, Hkv, D, cap = _attn_shapes(q, k_cache, v_cache, out)
-    for n, t in (("k_new", k_new), ("v_new", v_new), ("position_ids", position_ids), ("rope_cos", rope_cos),
-                 ("rope_sin", rope_sin)):
-        _cuda_contig(n, t)
-    _require(tuple(k_new.shape) == (B, Hkv, D) and v_new.shape == k_new.shape, "k_new/v_new must be [B, n_kv_head, D]")
-    _require(position_ids.dtype == torch.int32 and position_ids.numel() == B, "position_ids must be int32 [B]")
+    B, H, Hkv, D, cap = _step_inputs(q, k_cache, v_cache, k_new, v_new, position_ids, out)
+    dev = q.device
+    _on(dev, rope_cos=rope_cos, rope_sin=rope_sin)
     _require(rope_cos.dtype == torch.float32 and rope_sin.dtype == torch.float32 and rope_cos.dim() == 2
              and rope_cos.shape == rope_sin.shape and rope_cos.shape[1] == D, "rope tables must be fp32 [rows, D]")
     if scale is None:
         scale = D ** -0.5
     if workspace is None:
-        workspace = alloc_workspace(B, H, Hkv, D, cap, q.device)
-    st = load_library().decode_step_rope_fwd(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
-                                             _ptr(rope_cos), _ptr(rope_sin), rope_cos.shape[0], _ptr(position_ids),
-                                             B, H, Hkv, D, cap, float(scale), _ptr(out), _ptr(workspace),
-                                             workspace.numel(), int(max_kv_len_hint), _dtype_code(q),
-                                             _ptr(err_flag), _stream(q))
-    _check("decode_step_rope_fwd", st)
+        workspace = alloc_workspace(B, H, Hkv, D, cap, dev)
+    ws, ws_bytes = _workspace(workspace, dev)
+    _call("decode_step_rope_fwd", dev, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
+          _ptr(rope_cos), _ptr(rope_sin), rope_cos.shape[0], _ptr(position_ids), B, H, Hkv, D, cap, float(scale),
+          _ptr(out), ws, ws_bytes, int(max_kv_len_hint), _dtype_code(q), _err_ptr(err_flag, dev), _stream(q))
     return out
 
 
@@ -284,23 +323,36 @@ def decode_step_layers_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         return out
     _require(k_cache.shape[0] == layers and v_cache.shape == k_cache.shape and out.shape == q.shape,
              "every tensor needs the same leading layer count")
-    B, H, Hkv, D, cap = _attn_shapes(q[0], k_cache[0], v_cache[0], out[0])
-    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("out", out), ("k_new", k_new),
-                 ("v_new", v_new), ("position_ids", position_ids)):
-        _cuda_contig(n, t)
-    _require(tuple(k_new.shape) == (layers, B, Hkv, D) and v_new.shape == k_new.shape,
-             "k_new/v_new must be [layers, B, n_kv_head, D]")
-    _require(position_ids.dtype == torch.int32 and position_ids.numel() == B, "position_ids must be int32 [B]")
+    B, H, Hkv, D, cap = _step_inputs(q, k_cache, v_cache, k_new, v_new, position_ids, out, lead=(layers,))
+    dev = q.device
     if scale is None:
         scale = D ** -0.5
     if workspace is None:
-        workspace = alloc_workspace(B, H, Hkv, D, cap, q.device)
-    st = load_library().decode_step_layers_fwd(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
-                                               _ptr(position_ids), layers, B, H, Hkv, D, cap, float(scale),
-                                               _ptr(out), _ptr(workspace), workspace.numel(), int(max_kv_len_hint),
-                                               _dtype_code(q), _ptr(err_flag), _stream(q))
-    _check("decode_step_layers_fwd", st)
+        workspace = alloc_workspace(B, H, Hkv, D, cap, dev)
+    ws, ws_bytes = _workspace(workspace, dev)
+    _call("decode_step_layers_fwd", dev, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
+          _ptr(position_ids), layers, B, H, Hkv, D, cap, float(scale), _ptr(out), ws, ws_bytes,
+          int(max_kv_len_hint), _dtype_code(q), _err_ptr(err_flag, dev), _stream(q))
     return out
+
+
+def set_prefix_ready(on: bool) -> None:
+    """Ordering promise of this thread's later decode calls (see
+    da_set_prefix_ready in the C header): with B == 1 and a length bound, no
+    kernel still running when a call's kernel starts writes the cache rows the
+    call reads, so the kernel may copy its first tiles before waiting for the
+    previous kernel on the stream."""
+    load_library().da_set_prefix_ready(1 if on else 0)
+
+
+@contextlib.contextmanager
+def prefix_ready():
+    """set_prefix_ready(True) for the calls (or the stream capture) inside the block."""
+    set_prefix_ready(True)
+    try:
+        yield
+    finally:
+        set_prefix_ready(False)
 
 
 def test_skip_slot(slot: int) -> None:
@@ -324,12 +376,11 @@ def decode_attn_fwd_static_scratch(q: torch.Tensor, k_cache: torch.Tensor, v_cac
     if out is None:
         out = torch.empty_like(q)
     B, H, Hkv, D, cap = _attn_shapes(q, k_cache, v_cache, out)
-    _cuda_contig("kv_len", kv_len)
+    dev = q.device
+    _on(dev, kv_len=kv_len)
     _require(kv_len.dtype == torch.int32 and kv_len.numel() == B, "kv_len must be int32 [B]")
     if scale is None:
         scale = D ** -0.5
-    st = load_library().decode_attn_fwd_static_scratch(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), B, H,
-                                                       Hkv, D, cap, float(scale), _ptr(out), int(max_kv_len_hint),
-                                                       _dtype_code(q), _ptr(err_flag), _stream(q))
-    _check("decode_attn_fwd_static_scratch", st)
+    _call("decode_attn_fwd_static_scratch", dev, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), B, H, Hkv, D,
+          cap, float(scale), _ptr(out), int(max_kv_len_hint), _dtype_code(q), _err_ptr(err_flag, dev), _stream(q))
     return out

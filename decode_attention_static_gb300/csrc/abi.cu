@@ -115,6 +115,8 @@ thread_local cudaEvent_t t_event_before = nullptr;
 thread_local cudaEvent_t t_event_after = nullptr;
 // Failure-detection test hook (da_test_skip_slot) of this host thread.
 thread_local int t_skip_slot = -1;
+// Ordering promise (da_set_prefix_ready) of this host thread.
+thread_local int t_prefix_ready = 0;
 
 cudaError_t record_event(cudaEvent_t ev, cudaStream_t st) {
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -211,6 +213,7 @@ int decode_common(const void* q, const void* k_cache, const void* v_cache, void*
   // One sequence with an explicit bound: the bound is normally its length,
   // so the kernel issues its first tiles before reading the length.
   p.speculate = (B == 1 && max_kv_len_hint > 0) ? 1 : 0;
+  p.prefix_ready = (p.speculate && t_prefix_ready) ? 1 : 0;
   p.qscale = scale * kLog2e;
   p.out = static_cast<uint8_t*>(out);
   if (need > 0) {
@@ -342,6 +345,11 @@ int decode_attn_splits_for(int B, int n_head, int n_kv_head, int head_dim, int c
 
 int da_test_skip_slot(int slot) {
   da::t_skip_slot = slot < 0 ? -1 : slot;
+  return DA_OK;
+}
+
+int da_set_prefix_ready(int on) {
+  da::t_prefix_ready = on ? 1 : 0;
   return DA_OK;
 }
 

@@ -312,6 +312,7 @@ struct DecodeParams {
   int len_hint;            // host bound on the active lengths (<= capacity): L2 prefetch, early tiles
   int skip_slot;           // test hook: ring slot left unfilled in one CTA (< 0: none)
   int speculate;           // 1: len_hint is expected to be the exact length (early tiles are issued)
+  int prefix_ready;        // with speculate: the early tiles' cached rows may be read before the grid wait
   int cluster;             // CTAs per thread-block cluster along the split axis (divides splits)
   float qscale;            // softmax scale * log2(e)
   uint8_t* out;            // [B, n_head, D]

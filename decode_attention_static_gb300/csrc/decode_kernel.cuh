@@ -398,47 +398,16 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
   const int64_t head0 = (int64_t)b * H + (int64_t)g_kv * G;
   const int64_t kv_row0 = ((int64_t)b * p.n_kv_head + g_kv) * p.capacity;  // first cache row of this (b, g)
 
-  // Everything before pdl_wait() touches no memory the previous kernel on the
-  // stream may still write, except for L2 prefetches (L2 is coherent).
-  uint64_t policy = 0;
-  if (threadIdx.x == CT) {
-    policy = evict_first_policy();
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], CW);
-    }
-    *abort_flag = 0;
-    fence_mbar_init();
-    // Pull the first tiles this CTA will probably read into L2, with rows
-    // from the host's length bound (clamped to the cache): two tiles when one
-    // sequence gives each CTA a short chunk (every CTA's first tiles then land
-    // sooner, the rest streams behind them), else a ring's worth.
-    const int lh = p.len_hint;
-    const int ch = split_chunk(lh, p.splits, Shape::kTileRows);
-    const int pr0 = s * ch;
-    if (pr0 < lh) {
-      const int ahead = (p.B == 1 && ch <= 6 * Shape::kTileRows) ? min(2, kStages) : kStages;
-      const int rows = min(min(ch, lh - pr0), ahead * Shape::kTileRows);
-      for (int t0 = 0; t0 < rows; t0 += Shape::kTileRows) {
-        const int n = min(Shape::kTileRows, rows - t0);
-        const int64_t off = (kv_row0 + pr0 + t0) * Shape::kRowBytes;
-        prefetch_l2(p.k_cache + off, n * Shape::kRowBytes);
-        prefetch_l2(p.v_cache + off, n * Shape::kRowBytes);
-      }
-    }
-  }
-  __syncthreads();
-  pdl_wait();
-  // The next grid may be scheduled from here on: once it runs, every grid
-  // before this one has completed.
-  pdl_trigger();
-
+  uint64_t policy = 0;  // L2 eviction policy of the tile copies (producer lane)
+  enum : int { kSlotAll = 0, kSlotCached = 1, kSlotNew = 2 };
   const bool fused = p.k_new != nullptr;
   const bool rope = RP && fused && p.rope_cos != nullptr;  // instances with RP serve the rotary step
   const int64_t new_row = ((int64_t)b * p.n_kv_head + g_kv) * D;  // element offset into k_new
   // Ring slot u takes rows [tr0, tr0 + rows) of this CTA's K and V, the row
   // at Lx - 1 from k_new/v_new in the fused step (producer lane only).
-  auto issue = [&](int u, int tr0, int rows, int Lx) {
+  // `part` may split that in two: kSlotCached arms the slot's barrier for all
+  // of its bytes and copies the cached rows, kSlotNew copies the new row.
+  auto issue = [&](int u, int tr0, int rows, int Lx, int part) {
     // Test hook: leave one slot of one CTA unfilled (its waits then time out).
     if (u == p.skip_slot && s == 0 && b == 0 && g_kv == 0) return;
     const int stage = u % kStages;
@@ -446,15 +415,17 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
     const int cached = new_last ? rows - 1 : rows;
     uint8_t* kdst = smem + stage * Shape::kStageBytes;
     uint8_t* vdst = kdst + kTileBytes;
-    // With rotary embedding the producer warp has already stored the new row
-    // into this stage (rope_row): only the cached rows arrive by TMA.
-    mbar_arrive_expect_tx(&full[stage], 2u * (new_last && rope ? cached : rows) * Shape::kRowBytes);
-    if (cached > 0) {
-      const int64_t off = (kv_row0 + tr0) * Shape::kRowBytes;
-      bulk_load(kdst, p.k_cache + off, cached * Shape::kRowBytes, &full[stage], policy);
-      bulk_load(vdst, p.v_cache + off, cached * Shape::kRowBytes, &full[stage], policy);
+    if (part != kSlotNew) {
+      // With rotary embedding the producer warp has already stored the new row
+      // into this stage (rope_row): only the cached rows arrive by TMA.
+      mbar_arrive_expect_tx(&full[stage], 2u * (new_last && rope ? cached : rows) * Shape::kRowBytes);
+      if (cached > 0) {
+        const int64_t off = (kv_row0 + tr0) * Shape::kRowBytes;
+        bulk_load(kdst, p.k_cache + off, cached * Shape::kRowBytes, &full[stage], policy);
+        bulk_load(vdst, p.v_cache + off, cached * Shape::kRowBytes, &full[stage], policy);
+      }
     }
-    if (new_last && !rope) {
+    if (new_last && !rope && part != kSlotCached) {
       const int64_t off = new_row * 2;
       bulk_load(kdst + cached * Shape::kRowBytes, p.k_new + off, Shape::kRowBytes, &full[stage], policy);
       bulk_load(vdst + cached * Shape::kRowBytes, p.v_new + off, Shape::kRowBytes, &full[stage], policy);
@@ -494,26 +465,82 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
 
   // Early tiles: when the host's bound is expected to be the exact length
   // (p.speculate), the producer issues this CTA's first tiles for that length
-  // before the length itself has been read. They are kept if the length
-  // matches, else left to land and discarded (ring slots 0..spec-1).
-  int spec = 0;
-  int spec_new = -1;  // early slot holding the rotated row of the bound's last position
-  if (p.speculate) {
-    const int lh = p.len_hint;
-    const int chh = split_chunk(lh, p.splits, Shape::kTileRows);
-    const int r0h = min(s * chh, lh);
-    const int r1h = min(lh, r0h + chh);
-    spec = min((r1h - r0h + Shape::kTileRows - 1) / Shape::kTileRows, kStages);
-    if (warp == CW) {
+  // before the length itself has been read: slots 0..spec-1 take rows
+  // [r0h, r1h) of the bound's split. They are kept if the length matches,
+  // else left to land and discarded.
+  const int lh = p.len_hint;
+  const int chh = split_chunk(lh, p.splits, Shape::kTileRows);
+  const int r0h = min(s * chh, lh);
+  const int r1h = min(lh, r0h + chh);
+  const int spec = p.speculate ? min((r1h - r0h + Shape::kTileRows - 1) / Shape::kTileRows, kStages) : 0;
+  // With a ready prefix, the early tiles are copied before the grid wait when
+  // they are every CTA's whole chunk (short chunks, where the wait
+  // dominates); launches with longer chunks keep the L2 prefetch, since
+  // copies into shared memory then slow the previous kernel's streaming more
+  // than they gain.
+  const bool pre = p.prefix_ready && chh <= kStages * Shape::kTileRows;
+
+  // Everything before pdl_wait() touches no memory the previous kernel on the
+  // stream may still write, except for L2 prefetches (L2 is coherent) and,
+  // when the caller has declared the cached prefix ready (p.prefix_ready:
+  // no kernel still running writes rows [0, len_hint) of these caches other
+  // than the new row) and `pre` holds, the cached rows of the early tiles.
+  if (threadIdx.x == CT) {
+    policy = evict_first_policy();
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], CW);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    const int ch = chh;
+    const int pr0 = s * ch;
+    if (pre) {
+      // The early tiles' cached rows go straight into the ring; a slot whose
+      // new row is rotated first (rope) waits for the grid in full.
       for (int t = 0; t < spec; ++t) {
         const int tr0 = r0h + t * Shape::kTileRows;
         const int rows = min(Shape::kTileRows, r1h - tr0);
-        if (rope && tr0 + rows == lh) {
-          rope_row(lh - 1, t, rows - 1, false);  // not into the cache before the length is known
-          spec_new = t;
-        }
-        if (lane == 0) issue(t, tr0, rows, lh);
+        if (!(rope && tr0 + rows == lh)) issue(t, tr0, rows, lh, kSlotCached);
       }
+    } else if (pr0 < lh) {
+      // Pull the first tiles this CTA will probably read into L2, with rows
+      // from the host's length bound (clamped to the cache): two tiles when one
+      // sequence gives each CTA a short chunk (every CTA's first tiles then land
+      // sooner, the rest streams behind them), else a ring's worth.
+      const int ahead = (p.B == 1 && ch <= 6 * Shape::kTileRows) ? min(2, kStages) : kStages;
+      const int rows = min(min(ch, lh - pr0), ahead * Shape::kTileRows);
+      for (int t0 = 0; t0 < rows; t0 += Shape::kTileRows) {
+        const int n = min(Shape::kTileRows, rows - t0);
+        const int64_t off = (kv_row0 + pr0 + t0) * Shape::kRowBytes;
+        prefetch_l2(p.k_cache + off, n * Shape::kRowBytes);
+        prefetch_l2(p.v_cache + off, n * Shape::kRowBytes);
+      }
+    }
+  }
+  __syncthreads();
+  pdl_wait();
+  // The next grid may be scheduled from here on: once it runs, every grid
+  // before this one has completed.
+  pdl_trigger();
+
+  // Early tiles after the wait: all of them, or with a ready prefix the new
+  // rows of the slots issued above and the rotated slot.
+  int spec_new = -1;  // early slot holding the rotated row of the bound's last position
+  if (warp == CW) {
+    for (int t = 0; t < spec; ++t) {
+      const int tr0 = r0h + t * Shape::kTileRows;
+      const int rows = min(Shape::kTileRows, r1h - tr0);
+      const bool has_new = fused && tr0 + rows == lh;
+      if (pre && !(rope && has_new)) {
+        if (has_new && lane == 0) issue(t, tr0, rows, lh, kSlotNew);
+        continue;
+      }
+      if (rope && has_new) {
+        rope_row(lh - 1, t, rows - 1, false);  // not into the cache before the length is known
+        spec_new = t;
+      }
+      if (lane == 0) issue(t, tr0, rows, lh, kSlotAll);
     }
   }
   // A CTA leaving before its pipeline runs first lets the early tiles land.
@@ -631,7 +658,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
         const int tr0 = r0 + t * Shape::kTileRows;
         const int rows = min(Shape::kTileRows, r1 - tr0);
         if (rope && tr0 + rows == L) rope_row(L - 1, u, rows - 1, true);
-        if (lane == 0) issue(u, tr0, rows, L);
+        if (lane == 0) issue(u, tr0, rows, L, kSlotAll);
         next = u + 1;
       }
     } else if (lane == 0) {
@@ -646,7 +673,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
         }
         if (*reinterpret_cast<volatile int*>(abort_flag)) break;
         const int tr0 = r0 + t * Shape::kTileRows;
-        issue(u, tr0, min(Shape::kTileRows, r1 - tr0), L);
+        issue(u, tr0, min(Shape::kTileRows, r1 - tr0), L, kSlotAll);
         next = u + 1;
       }
     }

@@ -145,6 +145,28 @@ DA_API int decode_attn_splits_for(int B, int n_head, int n_kv_head, int head_dim
 DA_API int da_set_timing_events(void* event_before, void* event_after);
 
 /*
+ * Ordering promise for the decode calls of this host thread (default off).
+ * Every decode kernel waits, by programmatic dependent launch, for the
+ * kernel before it on the stream to complete before it reads its inputs.
+ * With on != 0 the caller promises, for every later call of this thread with
+ * B == 1 and max_kv_len_hint > 0, that no kernel that may still be running
+ * when the call's kernel starts writes the cache rows the call will read:
+ * rows [0, max_kv_len_hint) of k_cache and v_cache for decode_attn_fwd, rows
+ * [0, max_kv_len_hint - 1) for the fused steps (whose last row comes from
+ * k_new and v_new). The kernel then copies those rows of its first tiles into
+ * shared memory before that wait; q, the lengths, k_new, v_new and the rotary
+ * tables are still read after it. A decode loop meets the promise when the
+ * only kernels between two calls on the same caches complete before the next
+ * one starts: for instance the previous layer's call and the projections
+ * (kernels on this stream release their dependents only after their own wait,
+ * as this library's do). Back-to-back calls on the SAME caches (one layer,
+ * nothing in between) do not: the first writes row position into the rows the
+ * second reads. Breaking the promise gives wrong results, never a fault.
+ * Returns DA_OK.
+ */
+DA_API int da_set_prefix_ready(int on);
+
+/*
  * Failure-detection test hook. With slot >= 0, every later decode call made
  * by this host thread leaves ring slot `slot` of the first split of sequence
  * 0, KV head 0 unfilled: that CTA's pipeline waits run into their time limit

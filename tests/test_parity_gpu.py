@@ -295,3 +295,23 @@ def test_layers_call_matches_per_layer_calls(ora):
         kb, vb, o = oracle_step(ora, steps[l])
         assert np.array_equal(bits(kc[l]), kb) and np.array_equal(bits(vc[l]), vb)
         assert_close(out[l], o, f"layer {l}")
+
+
+def test_binding_checks_flags_and_counts_workspace_bytes(ora):
+    """The binding rejects an error flag that is not int32 and passes a
+    workspace's size in bytes whatever its element type."""
+    step = W.long_context(seed=18, kv_len=9000, capacity=9000)
+    kb, vb, ref = oracle_step(ora, step)
+    d = step.to("cuda")
+    with pytest.raises(ValueError):
+        da.kvcache_append(d.k_cache, d.v_cache, d.k_new, d.v_new, d.position_ids,
+                          err_flag=torch.zeros(1, dtype=torch.int64, device="cuda"))
+    da.kvcache_append(d.k_cache, d.v_cache, d.k_new, d.v_new, d.position_ids)
+    n = da.decode_attn_workspace_size(1, step.n_head, step.n_kv_head, step.head_dim, step.capacity)
+    assert n > 16
+    ws = torch.zeros((n + 15) // 16, 4, dtype=torch.float32, device="cuda")
+    out = da.decode_attn_fwd(d.q, d.k_cache, d.v_cache, d.kv_len.contiguous(), workspace=ws,
+                             max_kv_len_hint=step.capacity)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(d.k_cache), kb) and np.array_equal(bits(d.v_cache), vb)
+    assert_close(out, ref, "float32 workspace")
