@@ -35,6 +35,16 @@ def test_mha_sweep(ora, kv_len, fused):
     check_step(ora, W.mha_sweep(kv_len, seed=1), fused, what=f"MHA kv {kv_len}")
 
 
+@pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
+@pytest.mark.parametrize("kv_len", [2048, 3072, 5000, 6144])
+def test_mha_mid_lengths(ora, kv_len, fused):
+    """Prefixes between the sweep's lengths, where the plan may trade cluster
+    size for co-residency (idle splits included): one cluster per group."""
+    s, cs = da.splits_for(1, 16, 16, 128, kv_len, kv_len, torch.float16)
+    assert s == cs >= 2
+    check_step(ora, W.mha_sweep(kv_len, seed=kv_len % 97), fused, hint=kv_len, what=f"MHA kv {kv_len}")
+
+
 @pytest.mark.parametrize("kv_len", W.MHA_SWEEP_KV_LENS)
 def test_mha_sweep_nan_tail(ora, kv_len):
     check_step(ora, W.mha_sweep(kv_len, seed=2, extra_capacity=64), False, what=f"MHA kv {kv_len} + tail")
