@@ -65,8 +65,9 @@ def test_batched_streaming(ora, fused, seed):
 
 @pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
 def test_s2pro_generation(ora, fused):
-    """36 layers x 400 steps of append + attend; every 50th step (and the
-    last) checked against the oracle in every layer; final caches bit-exact."""
+    """36 layers x 400 steps of append + attend; final caches bit-exact; all
+    14,400 layer-steps checked against the oracle. The oracle of step i reads
+    the final cache: its rows below kv_len were already final at step i."""
     g = W.s2pro_generation(seed=6)
     dev = "cuda"
     shape = (g.layers, g.B, g.n_kv_head, g.capacity, g.head_dim)
@@ -75,8 +76,7 @@ def test_s2pro_generation(ora, fused):
     kc[:, :, :, :g.prompt] = g.k_prefix.to(dev)
     vc[:, :, :, :g.prompt] = g.v_prefix.to(dev)
     q, kn, vn = g.q.to(dev), g.k_new.to(dev), g.v_new.to(dev)
-    check_steps = sorted(set(range(0, g.steps, 50)) | {g.steps - 1})
-    outs = {}
+    outs = torch.empty((g.steps, g.layers, g.B, g.n_head, g.head_dim), dtype=q.dtype, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     ws = da.alloc_workspace(g.B, g.n_head, g.n_kv_head, g.head_dim, g.capacity)
     for i in range(g.steps):
@@ -84,14 +84,13 @@ def test_s2pro_generation(ora, fused):
         kv = pos + 1
         for layer in range(g.layers):
             if fused:
-                o = da.decode_step_fwd(q[i, layer], kc[layer], vc[layer], kn[i, layer], vn[i, layer], pos,
-                                       workspace=ws, max_kv_len_hint=g.position(i) + 1, err_flag=err)
+                da.decode_step_fwd(q[i, layer], kc[layer], vc[layer], kn[i, layer], vn[i, layer], pos,
+                                   out=outs[i, layer], workspace=ws, max_kv_len_hint=g.position(i) + 1,
+                                   err_flag=err)
             else:
                 da.kvcache_append(kc[layer], vc[layer], kn[i, layer], vn[i, layer], pos, err_flag=err)
-                o = da.decode_attn_fwd(q[i, layer], kc[layer], vc[layer], kv, workspace=ws,
-                                       max_kv_len_hint=g.position(i) + 1, err_flag=err)
-            if i in check_steps:
-                outs[(i, layer)] = o.clone()
+                da.decode_attn_fwd(q[i, layer], kc[layer], vc[layer], kv, out=outs[i, layer], workspace=ws,
+                                   max_kv_len_hint=g.position(i) + 1, err_flag=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     end = g.prompt + g.steps
@@ -100,11 +99,18 @@ def test_s2pro_generation(ora, fused):
     assert np.array_equal(bits(kc[:, :, :, :end]), bits(k_full)), "K cache prefix"
     assert np.array_equal(bits(vc[:, :, :, :end]), bits(v_full)), "V cache prefix"
     assert bool(torch.isnan(kc[:, :, :, end:].float()).all()) and bool(torch.isnan(vc[:, :, :, end:].float()).all())
-    for (i, layer), o in outs.items():
-        L = g.position(i) + 1
-        ref = ora.decode_attn(bits(g.q[i, layer]), bits(k_full[layer]), bits(v_full[layer]),
-                              np.array([L], np.int32), g.n_head, g.n_kv_head, g.dtype, threads=THREADS)
-        assert_close(o, ref, f"step {i} layer {layer}")
+    got = outs.cpu()
+    q_bits = bits(g.q)
+    worst = {"rel_frob": 0.0, "max_abs": 0.0}
+    for layer in range(g.layers):
+        kb, vb = bits(k_full[layer]), bits(v_full[layer])
+        for i in range(g.steps):
+            L = g.position(i) + 1
+            ref = ora.decode_attn(q_bits[i, layer], kb, vb, np.array([L], np.int32), g.n_head, g.n_kv_head,
+                                  g.dtype, threads=THREADS)
+            r = assert_close(got[i, layer], ref, f"step {i} layer {layer}")
+            worst = {k: max(worst[k], r[k]) for k in worst}
+    assert worst["rel_frob"] <= 5e-3
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])

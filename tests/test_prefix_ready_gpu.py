@@ -67,12 +67,13 @@ def test_kept_early_tiles_match_default_ordering_and_oracle(ora, name):
     assert_close(out1, ref, name)
 
 
-@pytest.mark.parametrize("delta", [-700, -1, 1, 64, 900])
-def test_discarded_early_tiles(ora, delta):
-    """Bound off the length: the early tiles (copied before the wait) are
-    discarded and the call is still exact."""
-    step = W.decode_step(1, 16, 16, 128, 6000, "f16", [4095], seed=77)
-    hint = 4096 + delta
+@pytest.mark.parametrize("L,delta", [(1024, -700), (1024, -1), (1024, 1), (1024, 64), (1024, 900),
+                                     (4096, -1), (4096, 900)])
+def test_discarded_early_tiles(ora, L, delta):
+    """Bound off the length: the early tiles (copied before the wait when the
+    bound's chunks are short) are discarded and the call is still exact."""
+    step = W.decode_step(1, 16, 16, 128, 6000, "f16", [L - 1], seed=77)
+    hint = L + delta
     kb, vb, ref = oracle_step(ora, step)
     _, out0, _ = _fused(step, hint, ready=False)
     d1, out1, err1 = _fused(step, hint, ready=True)
@@ -85,15 +86,15 @@ def test_discarded_early_tiles(ora, delta):
 def test_attention_call_with_ready_prefix(ora):
     """decode_attn_fwd reads rows [0, bound) before the wait: the append is
     finished (synchronised) before the call, so the promise holds."""
-    step = W.mha_sweep(4096, seed=78)
+    step = W.mha_sweep(1024, seed=78)
     kb, vb, ref = oracle_step(ora, step)
     d = step.to("cuda")
     da.kvcache_append(d.k_cache, d.v_cache, d.k_new, d.v_new, d.position_ids)
     torch.cuda.synchronize()
     lens = d.kv_len.contiguous()
-    out0 = da.decode_attn_fwd(d.q, d.k_cache, d.v_cache, lens, max_kv_len_hint=4096)
+    out0 = da.decode_attn_fwd(d.q, d.k_cache, d.v_cache, lens, max_kv_len_hint=1024)
     with da.prefix_ready():
-        out1 = da.decode_attn_fwd(d.q, d.k_cache, d.v_cache, lens, max_kv_len_hint=4096)
+        out1 = da.decode_attn_fwd(d.q, d.k_cache, d.v_cache, lens, max_kv_len_hint=1024)
     torch.cuda.synchronize()
     assert _same(out1, out0)
     assert_close(out1, ref, "attention call")
@@ -176,8 +177,9 @@ def test_layers_call_with_ready_prefix():
 def test_timeout_on_a_slot_issued_before_the_wait(ora, slot):
     """The test hook leaves an early slot (normally copied before the wait)
     unfilled: the call reports DA_DEVERR_TIMEOUT, NaN for that group only,
-    and the next call on the same context is correct."""
-    step = W.mha_sweep(4096, seed=110)
+    and the next call on the same context is correct. (kv 1024: two-tile
+    chunks, both early slots copied before the wait.)"""
+    step = W.mha_sweep(1024, seed=110)
     G = step.n_head // step.n_kv_head
     ws = da.alloc_workspace(1, step.n_head, step.n_kv_head, step.head_dim, step.capacity)
     d = step.to("cuda")
@@ -186,7 +188,7 @@ def test_timeout_on_a_slot_issued_before_the_wait(ora, slot):
     da.set_prefix_ready(True)
     try:
         out = da.decode_step_fwd(d.q, d.k_cache, d.v_cache, d.k_new, d.v_new, d.position_ids, workspace=ws,
-                                 max_kv_len_hint=4096, err_flag=err)
+                                 max_kv_len_hint=1024, err_flag=err)
         torch.cuda.synchronize()
     finally:
         da.test_skip_slot(-1)
@@ -198,6 +200,40 @@ def test_timeout_on_a_slot_issued_before_the_wait(ora, slot):
     _, _, ref = oracle_step(ora, step)
     assert_close(out[:, G:], ref[:, G:], "unaffected groups")
     da.workspace_init(ws)
-    _, out2, err2 = _fused(step, 4096, ready=True)
+    _, out2, err2 = _fused(step, 1024, ready=True)
     assert err2 == 0
     assert_close(out2, ref, "after the timeout")
+
+
+@pytest.mark.parametrize("hint_delta", [0, -100, 37])
+def test_rotary_step_d64_with_ready_prefix(ora, hint_delta):
+    """Rotary step at head_dim 64, 8 query / 2 KV heads, with the bound on and
+    off the length (the rotated slot issued after the wait, kept or dropped)."""
+    cap, pos = 2000, 1499
+    step = W.decode_step(1, 8, 2, 64, cap, "bf16", [pos], seed=120)
+    cos, sin = W.random_rope_tables(cap, 64, seed=121)
+    outs = []
+    for ready in (False, True):
+        d = step.to("cuda")
+        da.set_prefix_ready(ready)
+        try:
+            out = da.decode_step_rope_fwd(d.q, d.k_cache, d.v_cache, d.k_new, d.v_new, cos.cuda(), sin.cuda(),
+                                          d.position_ids, max_kv_len_hint=pos + 1 + hint_delta)
+        finally:
+            da.set_prefix_ready(False)
+        torch.cuda.synchronize()
+        outs.append((d, out))
+    (d0, o0), (d1, o1) = outs
+    assert _same(o1, o0)
+    assert _same(d1.k_cache, d0.k_cache) and _same(d1.v_cache, d0.v_cache)
+
+
+def test_batch_is_unaffected_by_the_promise(ora):
+    """The promise only changes single-sequence calls with a bound: a batch
+    gives the same bits either way."""
+    step = W.batched_streaming(seed=5)
+    hint = int(step.position_ids.max()) + 1
+    r0 = _fused(step, hint, ready=False)
+    r1 = _fused(step, hint, ready=True)
+    assert r0[2] == 0 and r1[2] == 0
+    assert _same(r1[1], r0[1])
