@@ -24,8 +24,8 @@
 //
 // Merge of the splits. The splits of one (b, g) group are launched as
 // thread-block clusters of `cluster` CTAs. Each CTA folds its warps' states
-// into one (m, l, acc) in shared memory and stores, through distributed
-// shared memory, each rank's slice of it into that rank; after one cluster
+// into one (m, l, acc), the thread folding an output storing it straight
+// into the rank that merges it (distributed shared memory); after one cluster
 // barrier every CTA merges its slice of the G x D outputs over all CTAs of
 // its cluster from its own shared memory. A group served by one
 // cluster writes `out` there and then; a group served by several clusters
@@ -613,6 +613,13 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
                                                           c < LPR / 2);
   }
 
+  // Cluster merge geometry: rank k of the cluster merges outputs
+  // [k * per, (k + 1) * per); its receive area holds every rank's (m, l) and
+  // every rank's share of that slice.
+  const int per = (E + CS - 1) / CS;
+  float* ml_in = recv;                 // [CS][2G]
+  float* acc_in = recv + CS * 2 * G;   // [CS][per]
+
   if (warp == CW) {
     // ---------------- producer warp ----------------
     if (fused && !rope && s == 0 && lane < D / 8) {
@@ -799,19 +806,40 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
       if (i < E) merge_warps<D, G, CW>(red, i / D, i % D, &vm[k], &vl[k], &va[k]);
     }
     const float nan = __int_as_float(0x7fc00000);
+    if (CS > 1) {
+      // Cluster plans: each folded value goes straight to the rank that
+      // merges it (distributed shared-memory stores), (m, l) to every rank.
 #pragma unroll
-    for (int k = 0; k < Shape::kPerThread; ++k) {
-      const int i = threadIdx.x + k * CT;
-      if (i < E) {
-        state[i] = failed ? nan : va[k];
-        if (i % D == 0) {
-          state[E + i / D] = failed ? nan : vm[k];
-          state[E + G + i / D] = vl[k];
+      for (int k = 0; k < Shape::kPerThread; ++k) {
+        const int i = threadIdx.x + k * CT;
+        if (i < E) {
+          const int kk = i / per;
+          st_cluster_f32(acc_in + rank * per + (i - kk * per), kk, failed ? nan : va[k]);
+          if (i % D == 0) {
+            const int g = i / D;
+            for (int r = 0; r < CS; ++r) {
+              st_cluster_f32(ml_in + rank * 2 * G + g, r, failed ? nan : vm[k]);
+              st_cluster_f32(ml_in + rank * 2 * G + G + g, r, vl[k]);
+            }
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < Shape::kPerThread; ++k) {
+        const int i = threadIdx.x + k * CT;
+        if (i < E) {
+          state[i] = failed ? nan : va[k];
+          if (i % D == 0) {
+            state[E + i / D] = failed ? nan : vm[k];
+            state[E + G + i / D] = vl[k];
+          }
         }
       }
     }
   }
-  __syncthreads();
+  // The cluster barrier below orders the pushes; a lone CTA reads its state.
+  if (CS == 1) __syncthreads();
 
   // ---------------- merge over the cluster ----------------
   // Rank k of the cluster merges outputs [k * per, (k + 1) * per). Every CTA
@@ -822,21 +850,9 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
   // (lane r holds rank r; the max and the sums are shuffle reductions), a
   // wide one one output per thread. Nothing is read remotely, so a CTA may
   // leave as soon as it has merged.
-  const int per = (E + CS - 1) / CS;  // outputs merged by each CTA of the cluster
   const int e0 = rank * per;
   const int e1 = min(E, e0 + per);
-  float* ml_in = recv;                 // [CS][2G]: (m, l) of every rank
-  float* acc_in = recv + CS * 2 * G;   // [CS][per]: every rank's share of this CTA's slice
   if (CS > 1) {
-    for (int t = threadIdx.x; t < CS * 2 * G; t += Shape::kThreads) {
-      const int k = t / (2 * G);
-      const int j = t - k * 2 * G;
-      st_cluster_f32(ml_in + rank * 2 * G + j, k, state[E + j]);
-    }
-    for (int i = threadIdx.x; i < E; i += Shape::kThreads) {
-      const int k = i / per;
-      st_cluster_f32(acc_in + rank * per + (i - k * per), k, state[i]);
-    }
     cluster_arrive_release();
     cluster_wait_acquire();
   }
