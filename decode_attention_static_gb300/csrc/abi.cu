@@ -152,31 +152,8 @@ int plan_for_device(int dtype, int B, int n_kv_head, int head_dim, int group, in
     }
   }
   int cs = 1;
-  int s = decode_attn_plan_splits(B, n_kv_head, head_dim, bound, sms, info.ctas_per_sm, fit, &cs);
+  const int s = decode_attn_plan_splits(B, n_kv_head, head_dim, bound, sms, info.ctas_per_sm, fit, &cs);
   if (s < 1) return s;
-  // One cluster of `fit` per group over a long prefix whose chunks stay short:
-  // the launch is latency-bound, and a smaller cluster size that leaves a
-  // quarter more clusters co-resident lets the next launch's clusters start
-  // (programmatic dependent launch) while this one drains. Long chunks keep
-  // `fit`, where the extra streaming CTAs matter more.
-  const int64_t tiles = ((int64_t)bound + tile_rows(head_dim) - 1) / tile_rows(head_dim);
-  if (B == 1 && cs == fit && fit > 2 && units * fit >= sms && tiles >= 2 * fit) {
-    int roomy = 1;
-    for (int c = fit - 1; c >= 2; --c) {
-      if (info.active_clusters[c] >= units + (units + 3) / 4) {
-        roomy = c;
-        break;
-      }
-    }
-    if (roomy >= 2 && (tiles + roomy - 1) / roomy <= kRoomyChunkTiles) {
-      int cs2 = 1;
-      const int s2 = decode_attn_plan_splits(B, n_kv_head, head_dim, bound, sms, info.ctas_per_sm, roomy, &cs2);
-      if (s2 >= 1 && cs2 == roomy) {
-        s = s2;
-        cs = cs2;
-      }
-    }
-  }
   *splits = s;
   *cluster = cs;
   return DA_OK;

@@ -31,9 +31,6 @@ constexpr int kMaxClusterSize = 16;
 // by one thread-block cluster (on-chip merge); longer prefixes are split
 // over every resident CTA and merged through the workspace.
 constexpr int kClusterTilesPerSplit = 4;
-// Longest chunk (tiles per split) for which a long-prefix cluster plan trades
-// cluster size for room to start the next launch early.
-constexpr int kRoomyChunkTiles = 8;
 // The workspace starts with one 32-bit arrival counter per (sequence, KV
 // head) group, in a fixed region so that calls of any shape find their
 // counters at the same place; split decoding is used only for at most

@@ -130,11 +130,7 @@ DA_API int decode_attn_workspace_init(void* workspace, size_t workspace_bytes, v
  * memory, no workspace; S larger: one partial per cluster goes through the
  * workspace and the last CTA of each group merges them, in the same launch.
  * The plan is decode_attn_plan_splits with this device's occupancy (the
- * largest cluster size of which one cluster per group is co-resident),
- * refined for one sequence whose long prefix gets one cluster per group:
- * when its chunks stay at most 8 tiles, the largest smaller cluster size that
- * leaves a quarter more clusters co-resident, so that the next launch's
- * clusters can start while this one drains.
+ * largest cluster size of which one cluster per group is co-resident).
  * Returns S >= 1 or a negative da_status.
  */
 DA_API int decode_attn_splits_for(int B, int n_head, int n_kv_head, int head_dim, int capacity,
