@@ -48,7 +48,7 @@ struct DecodeShape {
   static constexpr int kConsumerThreads = CW * 32;
   static constexpr int kThreads = kConsumerThreads + 32;             // + the producer warp
   static constexpr int kRowBytes = 2 * D;
-  static constexpr int kTileRows = kTileBytes / kRowBytes;           // 32 for D=128, 64 for D=64
+  static constexpr int kTileRows = kTileBytes / kRowBytes;           // 64 for D=128, 128 for D=64
   static constexpr int kVecs = DPL / 8;                              // 16-byte vectors per lane per row
   static constexpr int kLanesPerRow = D / DPL;
   static constexpr int kRowsPerStep = 32 / kLanesPerRow;             // rows a warp covers per step
