@@ -649,9 +649,10 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
       *reinterpret_cast<uint4*>(p.v_cache_w + dst) = *reinterpret_cast<const uint4*>(src + kTileBytes);
     }
     int next = keep ? spec : slot0;  // next ring slot to fill
-    if constexpr (RP) {
-      // The whole warp walks the slots (lane 0 waits and issues) so that it
-      // can store the rotated row into a stage right before it is issued.
+    if (RP && rope && r1 == L) {
+      // The CTA whose chunk ends at the new row: the whole warp walks the
+      // slots (lane 0 waits and issues) so that it can store the rotated row
+      // into a stage right before it is issued.
       for (int t = keep ? spec : 0; t < ntiles; ++t) {
         const int u = t + slot0;
         const int stage = u % kStages;
