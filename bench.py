@@ -294,13 +294,25 @@ def traffic_from_profiles(source_hash: str) -> dict | None:
         return None
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source without its comments and blank lines (string literals in
+    these sources hold no comment markers)."""
+    import re
+
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the CUDA sources' code (comments excluded), which ties the ncu
+    figures under profiles/ to the code they were taken on."""
     import hashlib
 
     h = hashlib.sha256()
     for f in sorted((ROOT / "decode_attention_static_gb300" / "csrc").glob("*")):
         h.update(f.name.encode())
-        h.update(f.read_bytes())
+        h.update(strip_comments(f.read_text()).encode())
     return h.hexdigest()[:16]
 
 

@@ -844,9 +844,9 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
 
   // ---------------- merge over the cluster ----------------
   // Rank k of the cluster merges outputs [k * per, (k + 1) * per). Every CTA
-  // pushes its (m, l) and, for each rank, the slice of its accumulator that
-  // rank merges into that rank's receive area (distributed shared-memory
-  // stores, no round trips); after one cluster barrier each CTA merges its
+  // has pushed its (m, l) and, for each rank, the slice of its accumulator
+  // that rank merges into that rank's receive area (distributed shared-memory
+  // stores made by the fold above); after one cluster barrier each CTA merges its
   // slice from its own shared memory: a narrow slice one output per 16 lanes
   // (lane r holds rank r; the max and the sums are shuffle reductions), a
   // wide one one output per thread. Nothing is read remotely, so a CTA may

@@ -73,3 +73,23 @@ def test_two_rank_max_and_aggregate():
         r = dict(results)
     assert r[0][0] == r[1][0] == 15.0
     assert r[0][1] == pytest.approx(2 * 10**9 * 10 / 0.015 / 1e9)
+
+
+def test_kernel_hash_ignores_comments_only():
+    """The ncu figures under profiles/ stay tied to the kernel code: a comment
+    edit keeps the hash, a code edit changes it."""
+    src = "int f(int x) {\n  // doubles x\n  return 2 * x; /* cheap */\n}\n"
+    assert bench.strip_comments(src) == bench.strip_comments(src.replace("doubles x", "twice x"))
+    assert bench.strip_comments(src) != bench.strip_comments(src.replace("2 * x", "3 * x"))
+    assert "//" not in bench.strip_comments(src) and "/*" not in bench.strip_comments(src)
+
+
+def test_profile_traffic_matches_current_kernel_code():
+    """When profiles/ holds ncu traffic for the current kernel code, it is the
+    algorithmic bytes plus at most 2% (no re-reads)."""
+    traffic = bench.traffic_from_profiles(bench.kernel_source_hash())
+    if traffic is None:
+        pytest.skip("profiles/ holds no ncu traffic for the current kernel code (bench reports null)")
+    for kv in bench.SWEEP:
+        algorithmic = bench.attend_bytes(1, bench.N_HEAD, bench.N_KV_HEAD, bench.HEAD_DIM, [kv])
+        assert 1.0 <= traffic[kv] / algorithmic < 1.02
