@@ -418,8 +418,9 @@ def run_ours(args) -> dict | None:
     # ---- decode-kernel launch duration ----
     n = len(step.calls)
     if step.fused:
-        # every launch of the timed region is a decode kernel: average duration
-        # = timed region / launches, per kv_len from the per-group timings
+        # every launch of the timed region is a decode kernel: the average
+        # launch duration is the timed region / its launches (the per-kv_len
+        # rows below take each kv_len's graph timed alone)
         per_call = [group_ms[g] / step.groups[g]["layers"] for g, _ in step.calls]
         kernel_timing = "timed region / decode launches (the fused step launches only the decode kernel)"
     else:
@@ -495,7 +496,7 @@ def run_ours(args) -> dict | None:
                       "decode_kernel_gbs": round(kb / (kms * 1e-3) / 1e9, 1)})
 
     k_bytes = sum(step.call_attend_bytes(i) for i in range(n))
-    k_ms = sum(per_call)
+    k_ms = ms_max / args.steps if step.fused else sum(per_call)
     achieved = k_bytes / (k_ms * 1e-3) / 1e9
     traffic = traffic_from_profiles(kernel_source_hash())
     traffic_per_launch = None

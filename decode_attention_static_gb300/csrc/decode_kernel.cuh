@@ -505,10 +505,14 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
       }
     } else if (pr0 < lh) {
       // Pull the first tiles this CTA will probably read into L2, with rows
-      // from the host's length bound (clamped to the cache): two tiles when one
-      // sequence gives each CTA a short chunk (every CTA's first tiles then land
-      // sooner, the rest streams behind them), else a ring's worth.
-      const int ahead = (p.B == 1 && ch <= 6 * Shape::kTileRows) ? min(2, kStages) : kStages;
+      // from the host's length bound (clamped to the cache): when one sequence
+      // gives each CTA a short chunk, one tile for chunks of at most two and
+      // two for chunks of at most six (every CTA's first tiles then land
+      // sooner and compete less with the previous kernel's streaming; the
+      // rest streams behind them), else a ring's worth.
+      const int ahead = (p.B == 1 && ch <= 2 * Shape::kTileRows)   ? 1
+                        : (p.B == 1 && ch <= 6 * Shape::kTileRows) ? min(2, kStages)
+                                                                   : kStages;
       const int rows = min(min(ch, lh - pr0), ahead * Shape::kTileRows);
       for (int t0 = 0; t0 < rows; t0 += Shape::kTileRows) {
         const int n = min(Shape::kTileRows, rows - t0);
