@@ -3,13 +3,12 @@ slot of one CTA unfilled, so that CTA's bounded pipeline waits run out
 (about a second each). The call must report DA_DEVERR_TIMEOUT, publish NaN
 for the affected group only, and leave the context usable: the next call on
 the same stream, with the workspace zeroed again, is correct."""
-import numpy as np
 import pytest
 import torch
 
 import decode_attention_static_gb300 as da
 from decode_attention_static_gb300 import workloads as W
-from gpu_helpers import assert_close, bits, oracle_step
+from gpu_helpers import assert_close, oracle_step
 
 pytestmark = pytest.mark.gpu
 
