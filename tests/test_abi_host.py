@@ -197,3 +197,27 @@ def test_plain_c_program_uses_the_library(lib, tmp_path):
                    check=True, capture_output=True, text=True)
     out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
     assert (int(out[0]), int(out[1])) == da.plan_splits(1, 16, 128, 8192, 152, 2)
+
+
+@pytest.mark.parametrize("entry", ["decode_attn_fwd", "decode_step_fwd", "decode_step_rope_fwd",
+                                   "decode_step_layers_fwd", "kvcache_append", "decode_attn_fwd_static_scratch"])
+def test_binding_rejects_host_tensors_before_any_call(entry):
+    """Every binding entry point checks its tensors (device, contiguity) before
+    it reaches the library: host tensors raise ValueError, nothing runs."""
+    f16 = torch.float16
+    q = torch.zeros(1, 4, 64, dtype=f16)
+    kc = torch.zeros(1, 1, 8, 64, dtype=f16)
+    kn = torch.zeros(1, 1, 64, dtype=f16)
+    pos = torch.zeros(1, dtype=torch.int32)
+    calls = {
+        "decode_attn_fwd": lambda: da.decode_attn_fwd(q, kc, kc, pos),
+        "decode_step_fwd": lambda: da.decode_step_fwd(q, kc, kc, kn, kn, pos),
+        "decode_step_rope_fwd": lambda: da.decode_step_rope_fwd(q, kc, kc, kn, kn, torch.zeros(8, 64),
+                                                                torch.zeros(8, 64), pos),
+        "decode_step_layers_fwd": lambda: da.decode_step_layers_fwd(q[None], kc[None], kc[None], kn[None], kn[None],
+                                                                    pos),
+        "kvcache_append": lambda: da.kvcache_append(kc, kc, kn, kn, pos),
+        "decode_attn_fwd_static_scratch": lambda: da.decode_attn_fwd_static_scratch(q, kc, kc, pos),
+    }
+    with pytest.raises(ValueError):
+        calls[entry]()
