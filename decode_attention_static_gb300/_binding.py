@@ -11,6 +11,7 @@ from __future__ import annotations
 import contextlib
 import ctypes
 import pathlib
+import threading
 
 import torch
 
@@ -336,6 +337,9 @@ def decode_step_layers_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     return out
 
 
+_thread_state = threading.local()  # mirror of the library's per-thread ordering promise
+
+
 def set_prefix_ready(on: bool) -> None:
     """Ordering promise of this thread's later decode calls (see
     da_set_prefix_ready in the C header): with B == 1 and a length bound, no
@@ -343,16 +347,19 @@ def set_prefix_ready(on: bool) -> None:
     call reads, so the kernel may copy its first tiles before waiting for the
     previous kernel on the stream."""
     load_library().da_set_prefix_ready(1 if on else 0)
+    _thread_state.prefix_ready = bool(on)
 
 
 @contextlib.contextmanager
 def prefix_ready():
-    """set_prefix_ready(True) for the calls (or the stream capture) inside the block."""
+    """set_prefix_ready(True) for the calls (or the stream capture) inside the
+    block; the thread's previous setting comes back on exit (blocks nest)."""
+    before = getattr(_thread_state, "prefix_ready", False)
     set_prefix_ready(True)
     try:
         yield
     finally:
-        set_prefix_ready(False)
+        set_prefix_ready(before)
 
 
 def test_skip_slot(slot: int) -> None:

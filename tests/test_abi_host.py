@@ -221,3 +221,17 @@ def test_binding_rejects_host_tensors_before_any_call(entry):
     }
     with pytest.raises(ValueError):
         calls[entry]()
+
+
+def test_prefix_ready_blocks_nest_and_restore(lib):
+    """The binding's prefix_ready() block restores the thread's previous
+    setting (host-side state only; no GPU call)."""
+    from decode_attention_static_gb300 import _binding as B
+
+    da.set_prefix_ready(False)
+    with da.prefix_ready():
+        assert B._thread_state.prefix_ready
+        with da.prefix_ready():
+            assert B._thread_state.prefix_ready
+        assert B._thread_state.prefix_ready
+    assert not B._thread_state.prefix_ready
