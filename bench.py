@@ -656,7 +656,7 @@ def attend_only(torch, da, device, l2_bytes: int) -> list:
 def other_configs(torch, da, device, l2_bytes: int) -> dict:
     """The tiny GQA step, the batched streaming step and S2-Pro-shaped
     generation layer-steps (36 layers of 32 / 8 heads, bf16, capacity 32768)."""
-    from decode_attention_static_gb300 import workloads as W
+    import workloads as W
 
     res = {}
     flush_buf = torch.empty(3 * l2_bytes // 4 + 1, dtype=torch.int32, device=device)
@@ -736,7 +736,7 @@ def other_configs(torch, da, device, l2_bytes: int) -> dict:
 
 def cpu_sample(n_heads: int = N_HEAD, seed: int = 0):
     """One layer-step per kv_len of the sweep on the host (first n_heads heads)."""
-    from decode_attention_static_gb300 import workloads as W
+    import workloads as W
 
     items = []
     for kv in SWEEP:

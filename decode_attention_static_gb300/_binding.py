@@ -315,7 +315,9 @@ def decode_step_layers_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                            scale: float | None = None, workspace: torch.Tensor | None = None,
                            max_kv_len_hint: int = 0, err_flag: torch.Tensor | None = None) -> torch.Tensor:
     """decode_step_fwd for every layer of [layers, ...]-stacked inputs and
-    caches in one call (layer l uses q[l], k_cache[l], ..., writes out[l])."""
+    caches in one launch (layer l uses q[l], k_cache[l], ..., writes out[l]);
+    the layers are independent, a batch of layers * B sequences. A workspace
+    must hold decode_attn_workspace_size(layers * B, ...) bytes."""
     if out is None:
         out = torch.empty_like(q)
     _require(q.dim() == 4 and k_cache.dim() == 5, "q must be [layers, B, H, D] and caches [layers, B, Hkv, cap, D]")
@@ -329,7 +331,7 @@ def decode_step_layers_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     if scale is None:
         scale = D ** -0.5
     if workspace is None:
-        workspace = alloc_workspace(B, H, Hkv, D, cap, dev)
+        workspace = alloc_workspace(layers * B, H, Hkv, D, cap, dev)
     ws, ws_bytes = _workspace(workspace, dev)
     _call("decode_step_layers_fwd", dev, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
           _ptr(position_ids), layers, B, H, Hkv, D, cap, float(scale), _ptr(out), ws, ws_bytes,

@@ -159,11 +159,15 @@ int plan_for_device(int dtype, int B, int n_kv_head, int head_dim, int group, in
   return DA_OK;
 }
 
+// One decode launch over B sequences. `lens` has lens_period entries (B, or
+// a divisor of B when several layers of one batch share their lengths:
+// sequence b reads lens[b % lens_period]).
 int decode_common(const void* q, const void* k_cache, const void* v_cache, void* k_cache_w, void* v_cache_w,
                   const void* k_new, const void* v_new, const int32_t* lens, int lens_are_positions, int B,
                   int n_head, int n_kv_head, int head_dim, int capacity, float scale, void* out, void* workspace,
                   size_t workspace_bytes, int max_kv_len_hint, int dtype, int32_t* err_flag, void* stream,
-                  const float* rope_cos = nullptr, const float* rope_sin = nullptr, int rope_rows = 0) {
+                  const float* rope_cos = nullptr, const float* rope_sin = nullptr, int rope_rows = 0,
+                  int lens_period = 0) {
   int rc = check_sizes(B, n_head, n_kv_head, head_dim, capacity, dtype);
   if (rc != DA_OK) return rc;
   if (B == 0) return DA_OK;
@@ -199,6 +203,7 @@ int decode_common(const void* q, const void* k_cache, const void* v_cache, void*
   p.v_new = static_cast<const uint8_t*>(v_new);
   p.lens = lens;
   p.lens_are_positions = lens_are_positions;
+  p.lens_period = lens_period > 0 ? lens_period : B;
   p.B = B;
   p.n_head = n_head;
   p.n_kv_head = n_kv_head;
@@ -408,24 +413,12 @@ int decode_step_layers_fwd(const void* q, void* k_cache, void* v_cache, const vo
                            int max_kv_len_hint, int dtype, int32_t* err_flag, void* stream) {
   if (layers < 0) return DA_ERR_SHAPE;
   if (layers == 0 || B == 0) return DA_OK;
-  int rc = da::check_sizes(B, n_head, n_kv_head, head_dim, capacity, dtype);
-  if (rc != DA_OK) return rc;
-  const size_t es = 2;  // bytes per element of both storage types
-  const size_t q_stride = (size_t)B * n_head * head_dim * es;
-  const size_t cache_stride = (size_t)B * n_kv_head * capacity * head_dim * es;
-  const size_t new_stride = (size_t)B * n_kv_head * head_dim * es;
-  for (int l = 0; l < layers; ++l) {
-    const size_t lq = (size_t)l * q_stride, lc = (size_t)l * cache_stride, ln = (size_t)l * new_stride;
-    auto at = [](const void* base, size_t off) -> const uint8_t* {
-      return base ? static_cast<const uint8_t*>(base) + off : nullptr;
-    };
-    auto at_w = [](void* base, size_t off) -> uint8_t* { return base ? static_cast<uint8_t*>(base) + off : nullptr; };
-    rc = da::decode_common(at(q, lq), at(k_cache, lc), at(v_cache, lc), at_w(k_cache, lc), at_w(v_cache, lc),
-                           at(k_new, ln), at(v_new, ln), position_ids, 1, B, n_head, n_kv_head, head_dim, capacity,
-                           scale, at_w(out, lq), workspace, workspace_bytes, max_kv_len_hint, dtype, err_flag, stream);
-    if (rc != DA_OK) return rc;
-  }
-  return DA_OK;
+  if ((int64_t)layers * B > 65535) return DA_ERR_SHAPE;
+  // [layers, B, ...] stacks are [layers * B, ...] batches whose sequence
+  // l * B + b has the length of sequence b: every layer in one launch.
+  return da::decode_common(q, k_cache, v_cache, k_cache, v_cache, k_new, v_new, position_ids, 1, layers * B, n_head,
+                           n_kv_head, head_dim, capacity, scale, out, workspace, workspace_bytes, max_kv_len_hint,
+                           dtype, err_flag, stream, nullptr, nullptr, 0, B);
 }
 
 }  // extern "C"

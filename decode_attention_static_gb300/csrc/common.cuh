@@ -305,6 +305,7 @@ struct DecodeParams {
   const uint8_t* v_new;
   const int32_t* lens;     // kv_len, or position_ids when lens_are_positions
   int lens_are_positions;
+  int lens_period;         // entries of `lens`: sequence b reads lens[b % lens_period]
   int B, n_head, n_kv_head, capacity, splits;
   const float* rope_cos;   // fused step with rotary embedding: tables [rope_rows, D] (else null)
   const float* rope_sin;
@@ -325,7 +326,7 @@ struct DecodeParams {
 // Active length of sequence b, or -1 when its input is out of range
 // (setting the matching error bit in *err).
 __device__ __forceinline__ int sequence_length(const DecodeParams& p, int b, int32_t* err_bits) {
-  const int v = p.lens[b];
+  const int v = p.lens[p.lens_period == p.B ? b : b % p.lens_period];
   if (p.lens_are_positions) {
     if (v < 0 || v >= p.capacity) {
       *err_bits = kErrPosition | kErrKvLen;

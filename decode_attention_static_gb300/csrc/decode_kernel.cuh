@@ -125,15 +125,18 @@ __device__ __forceinline__ void merge_warps(const float* red, int g, int d, floa
 // barrier, it publishes every partial the CTA wrote before the barrier and,
 // for the last arrival, makes every other CTA's partials visible to the
 // threads that pass the next barrier (no separate fences).
-// A count already at or past `arrivals` means the counter was not zero: that
-// is reported as kErrWorkspace and the CTA does not merge.
+// A count already at or past `arrivals` means the counter was not zero when
+// the call started: that is reported as kErrWorkspace and returns -1, and the
+// caller writes NaN rows for the group (its merge cannot be trusted). The
+// counter is left as it is, so that every later call on it fails the same
+// visible way until the caller zero-fills it.
 __device__ __forceinline__ int arrive_count(unsigned int* counter, int arrivals, int32_t* err_flag) {
   unsigned int before;
   asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(before) : "l"(counter) : "memory");
   if (before + 1u < (unsigned int)arrivals) return 0;
   if (before + 1u > (unsigned int)arrivals) {
     if (err_flag) atomicOr(err_flag, kErrWorkspace);
-    return 0;
+    return -1;
   }
   atomicExch(counter, 0u);
   return 1;
@@ -937,9 +940,13 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
       *reinterpret_cast<volatile int*>(last_flag) = last;
     }
     __syncthreads();
-    if (*reinterpret_cast<volatile int*>(last_flag)) {
+    const int last = *reinterpret_cast<volatile int*>(last_flag);
+    if (last > 0) {
       // the ring is idle now
       merge_partials<T, D, G, Shape::kThreads>(p, head0, nclusters, p.splits / CS, reinterpret_cast<float*>(smem));
+    } else if (last < 0) {
+      for (int i = threadIdx.x; i < E; i += Shape::kThreads)
+        reinterpret_cast<uint16_t*>(p.out)[head0 * D + i] = S::kNaN;
     }
   }
 }

@@ -21,17 +21,18 @@ void* g_scratch_ptr[kMaxDevices] = {};
 std::mutex g_scratch_mutex;
 
 // Device address of g_static_scratch on the current device, looked up once
-// per device with that device current; the same set-up zero-fills the
-// arrival counters at the start of the array on `stream` (ahead of the
-// call's kernel). Returns DA_OK or DA_ERR_CUDA.
+// per device with that device current. The look-up is refused while `stream`
+// is being captured (it may load the library's device code, which a capture
+// does not allow). Returns DA_OK or DA_ERR_CUDA.
 int scratch_address(void** out, cudaStream_t stream) {
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices) return DA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
   if (!g_scratch_ptr[device]) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return DA_ERR_CUDA;
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) return DA_ERR_CUDA;
-    if (cudaMemsetAsync(ptr, 0, da::kCounterBytes, stream) != cudaSuccess) return DA_ERR_CUDA;
     g_scratch_ptr[device] = ptr;
   }
   *out = g_scratch_ptr[device];
@@ -57,6 +58,12 @@ extern "C" int decode_attn_fwd_static_scratch(const void* q, const void* k_cache
   if (need > 0) {
     const int rc = scratch_address(&scratch, static_cast<cudaStream_t>(stream));
     if (rc != DA_OK) return rc;
+    // This call's arrival counters (one per sequence and KV head, at the start
+    // of the array) start at zero whatever an earlier call left there: an
+    // overlapping or interrupted call cannot spoil the calls after it.
+    if (cudaMemsetAsync(scratch, 0, (size_t)B * n_kv_head * sizeof(unsigned int), static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+      return DA_ERR_CUDA;
   }
   return decode_attn_fwd(q, k_cache, v_cache, kv_len, B, n_head, n_kv_head, head_dim, capacity, scale, out, scratch,
                          need > 0 ? (size_t)DA_STATIC_SCRATCH_BYTES : 0, max_kv_len_hint, dtype, err_flag, stream);

@@ -73,7 +73,7 @@ typedef enum {
 #define DA_DEVERR_KV_LEN 1u   /* some kv_len[b] outside [1, capacity]: rows of b are NaN */
 #define DA_DEVERR_POSITION 2u /* some position_ids[b] outside [0, capacity): write skipped */
 #define DA_DEVERR_TIMEOUT 4u  /* a pipeline wait hit its time limit: rows are NaN */
-#define DA_DEVERR_WORKSPACE 8u /* the workspace counters were not zero: outputs not written */
+#define DA_DEVERR_WORKSPACE 8u /* the workspace counters were not zero: rows of the group are NaN */
 
 /* Human-readable name of a da_status value (static string). */
 DA_API const char* da_status_string(int status);
@@ -114,8 +114,10 @@ DA_API int decode_attn_plan_splits(int B, int n_kv_head, int head_dim, int max_k
  * sequence and KV head), followed by fp32 per-cluster partials
  * [B, n_head, S / cluster, head_dim + 2]. It must be zero-filled once before
  * its first use (decode_attn_workspace_init, or any memset); every call that
- * completes leaves it ready for the next call of any shape. After a
- * DA_DEVERR_TIMEOUT or DA_DEVERR_WORKSPACE, zero it again.
+ * completes leaves it ready for the next call of any shape. Calls that
+ * overlap on one workspace can leave a counter non-zero: a later call then
+ * merges that group early or writes NaN rows with DA_DEVERR_WORKSPACE. After
+ * a DA_DEVERR_TIMEOUT or DA_DEVERR_WORKSPACE, or an overlap, zero it again.
  */
 DA_API size_t decode_attn_workspace_size(int B, int n_head, int n_kv_head, int head_dim, int capacity);
 
@@ -251,15 +253,21 @@ DA_API int decode_step_rope_fwd(const void* q, void* k_cache, void* v_cache, con
  *   q, out          [layers, B, n_head, head_dim]
  *   k_cache, v_cache [layers, B, n_kv_head, capacity, head_dim]
  *   k_new, v_new    [layers, B, n_kv_head, head_dim]
- * all contiguous; position_ids [B] (the same step for every layer). The
- * layers are launched in order on `stream`, each allowed to start its
- * prologue while the previous one drains (programmatic dependent launch);
- * they share the workspace, which is safe because each launch merges before
- * the next one touches it. For a caller that holds every layer's inputs at
- * once (benchmarks, replays captured in one CUDA graph). Validation as
- * decode_step_fwd; every layer has the same sizes and (strides being
- * multiples of 16 bytes) the same alignment, so an invalid argument is
- * reported before the first launch. layers < 0 gives DA_ERR_SHAPE,
+ * all contiguous; position_ids [B] (the same step for every layer).
+ * Every layer's inputs are given at once, so no layer depends on another:
+ * the stacks are one batch of layers * B sequences (sequence l * B + b has
+ * position position_ids[b]) and the whole call is ONE launch of the decode
+ * kernel, with no per-layer launch cost. For a caller that holds every
+ * layer's inputs at once (replays, benchmarks, several independent models or
+ * requests stacked on a leading axis); in a model whose layer l + 1 query
+ * depends on layer l's output, call decode_step_fwd per layer instead.
+ * Results equal decode_step_fwd on the flattened [layers * B, ...] batch with
+ * position_ids repeated per layer, bit for bit.
+ *   workspace   at least decode_attn_workspace_size(layers * B, n_head,
+ *               n_kv_head, head_dim, capacity) bytes
+ * Validation as decode_step_fwd, all of it before the launch: an invalid
+ * argument enqueues nothing, and a launch failure (DA_ERR_CUDA) leaves every
+ * layer untouched. layers < 0 or layers * B > 65535 gives DA_ERR_SHAPE,
  * layers == 0 does nothing.
  */
 DA_API int decode_step_layers_fwd(const void* q, void* k_cache, void* v_cache, const void* k_new,
@@ -285,19 +293,24 @@ DA_API int decode_step_layers_fwd(const void* q, void* k_cache, void* v_cache, c
  * is allocated or freed by the call.
  *
  * - The first call on a device that needs scratch looks up that array's
- *   device address (cudaGetSymbolAddress, with that device current) and
- *   zero-fills its arrival counters on `stream`; make that first call before
- *   any stream capture on the device.
+ *   device address (cudaGetSymbolAddress, with that device current) and keeps
+ *   it for the life of the process; make that first call before any stream
+ *   capture on the device (a first call made while `stream` is capturing
+ *   returns DA_ERR_CUDA). A device reset (cudaDeviceReset) is not supported
+ *   afterwards.
  * - Arguments whose split plan needs more scratch than
  *   DA_STATIC_SCRATCH_BYTES (decode_attn_workspace_size-style need for this
  *   call's max_kv_len_hint) are rejected with DA_ERR_SHAPE before anything is
  *   enqueued; use decode_attn_fwd with your own workspace for those.
  * - Every call on a device shares the one array and leaves its partials in
- *   it. The kernels write every partial they later read, and every completed
- *   call leaves the arrival counters at zero again, so nothing has to be
- *   cleared between calls; but calls that overlap on the GPU (different
- *   streams without ordering, or different host threads) race on the array
- *   and give wrong results: keep such calls ordered.
+ *   it. A call that needs scratch first zero-fills its own arrival counters
+ *   on `stream` (a cudaMemsetAsync of 4 * B * n_kv_head bytes), and its
+ *   kernels write every partial they later read, so each call is correct
+ *   whatever an earlier call left in the array. Calls that overlap on the GPU
+ *   (different streams without ordering, or different host threads) race on
+ *   the array: their outputs may be wrong, NaN (with DA_DEVERR_WORKSPACE) or
+ *   left unwritten. Keep such calls ordered; the first ordered call after an
+ *   overlap is correct again, with nothing to reset.
  * Otherwise identical to decode_attn_fwd, including results bit for bit.
  */
 DA_API int decode_attn_fwd_static_scratch(const void* q, const void* k_cache, const void* v_cache,

@@ -9,7 +9,7 @@ import numpy as np
 import torch
 
 import decode_attention_static_gb300 as da
-from decode_attention_static_gb300 import workloads as W
+import workloads as W
 
 # fp16/bf16 inputs with fp32 accumulation against the fp64 oracle.
 REL_FROB_TOL = 5e-3

@@ -18,7 +18,7 @@ import numpy as np
 import torch
 import torch.nn.functional as F
 
-from decode_attention_static_gb300 import workloads as W
+import workloads as W
 
 F16_NAN = 0x7E00
 BF16_NAN = 0x7FC0

@@ -136,14 +136,17 @@ def test_decode_step_and_append_reject_bad_arguments(lib):
 
 
 def test_decode_step_layers_rejects_bad_arguments(lib):
-    def layers_call(layers=2, k_new=A, D=128):
-        return lib.decode_step_layers_fwd(A, A, A, k_new, A, A, layers, 1, 32, 8, D, 1024, 0.1, A, A, 1 << 30, 0, 1,
+    def layers_call(layers=2, k_new=A, D=128, B=1):
+        return lib.decode_step_layers_fwd(A, A, A, k_new, A, A, layers, B, 32, 8, D, 1024, 0.1, A, A, 1 << 30, 0, 1,
                                           None, None)
 
     assert layers_call(layers=-1) == -2
     assert layers_call(layers=0) == 0
     assert layers_call(k_new=None) == -1
     assert layers_call(D=96) == -3
+    assert layers_call(k_new=A + 4) == -6
+    # the stack is one batch of layers * B sequences (the grid's z extent)
+    assert layers_call(layers=300, B=300) == -2
 
 
 def test_decode_step_rope_rejects_bad_tables(lib):

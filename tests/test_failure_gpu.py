@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import decode_attention_static_gb300 as da
-from decode_attention_static_gb300 import workloads as W
+import workloads as W
 from gpu_helpers import assert_close, oracle_step
 
 pytestmark = pytest.mark.gpu

@@ -4,7 +4,7 @@ generator that feeds both the oracle and the CUDA path (CPU only)."""
 import json
 import pathlib
 
-from decode_attention_static_gb300 import workloads as W
+import workloads as W
 
 GOLD = json.loads((pathlib.Path(__file__).parent / "golden" / "kv_len_from_position.json").read_text())
 

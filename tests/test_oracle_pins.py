@@ -11,7 +11,7 @@ def test_oracle_pin(ora, pin):
 
 def test_openmp_threads_do_not_change_results(ora):
     import numpy as np
-    from decode_attention_static_gb300 import workloads as W
+    import workloads as W
 
     s = W.decode_step(2, 8, 2, 64, 300, "bf16", [299, 130], seed=1)
     args = (W.raw_bits(s.q), W.raw_bits(s.k_cache), W.raw_bits(s.v_cache), s.position_ids.numpy(),

@@ -2,12 +2,14 @@
 the seeded synthetic workloads, at full size, plus edge cases. Tolerances:
 rel-Frobenius <= 5e-3 and max-abs <= 2e-2 for the attention output; the
 cache append is compared bit for bit, NaN tail included."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
 
 import decode_attention_static_gb300 as da
-from decode_attention_static_gb300 import workloads as W
+import workloads as W
 from gpu_helpers import THREADS, assert_close, bits, check_step, gpu_step, oracle_step
 
 pytestmark = pytest.mark.gpu
@@ -63,11 +65,13 @@ def test_batched_streaming(ora, fused, seed):
     check_step(ora, step, fused, what="batched streaming")
 
 
-@pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
-def test_s2pro_generation(ora, fused):
-    """36 layers x 400 steps of append + attend; final caches bit-exact; all
-    14,400 layer-steps checked against the oracle. The oracle of step i reads
-    the final cache: its rows below kv_len were already final at step i."""
+@pytest.mark.parametrize("path", ["append+attend", "fused_step", "layers_call"])
+def test_s2pro_generation(ora, path):
+    """36 layers x 400 steps of append + attend (two calls per layer, one fused
+    call per layer, or one decode_step_layers_fwd launch for all 36 layers of
+    a step); final caches bit-exact; all 14,400 layer-steps checked against
+    the oracle. The oracle of step i reads the final cache: its rows below
+    kv_len were already final at step i."""
     g = W.s2pro_generation(seed=6)
     dev = "cuda"
     shape = (g.layers, g.B, g.n_kv_head, g.capacity, g.head_dim)
@@ -78,12 +82,16 @@ def test_s2pro_generation(ora, fused):
     q, kn, vn = g.q.to(dev), g.k_new.to(dev), g.v_new.to(dev)
     outs = torch.empty((g.steps, g.layers, g.B, g.n_head, g.head_dim), dtype=q.dtype, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    ws = da.alloc_workspace(g.B, g.n_head, g.n_kv_head, g.head_dim, g.capacity)
+    ws = da.alloc_workspace(g.layers * g.B, g.n_head, g.n_kv_head, g.head_dim, g.capacity)
     for i in range(g.steps):
         pos = torch.full((g.B,), g.position(i), dtype=torch.int32, device=dev)
         kv = pos + 1
+        if path == "layers_call":
+            da.decode_step_layers_fwd(q[i], kc, vc, kn[i], vn[i], pos, out=outs[i], workspace=ws,
+                                      max_kv_len_hint=g.position(i) + 1, err_flag=err)
+            continue
         for layer in range(g.layers):
-            if fused:
+            if path == "fused_step":
                 da.decode_step_fwd(q[i, layer], kc[layer], vc[layer], kn[i, layer], vn[i, layer], pos,
                                    out=outs[i, layer], workspace=ws, max_kv_len_hint=g.position(i) + 1,
                                    err_flag=err)
@@ -288,9 +296,11 @@ def test_small_workspace_is_rejected():
     assert e.value.status == -4
 
 
-def test_layers_call_matches_per_layer_calls(ora):
+def test_layers_call_is_one_batched_launch(ora):
     """decode_step_layers_fwd over stacked layers gives, bit for bit, the
-    caches and outputs of one decode_step_fwd per layer, and the oracle's."""
+    caches and outputs of one decode_step_fwd on the flattened
+    [layers * B, ...] batch (positions repeated per layer), and every layer
+    matches the oracle."""
     layers, B, H, Hkv, D, cap, dt = 6, 2, 32, 8, 128, 1000, "bf16"
     pos = [999, 400]
     steps = [W.decode_step(B, H, Hkv, D, cap, dt, pos, seed=60 + l) for l in range(layers)]
@@ -300,17 +310,49 @@ def test_layers_call_matches_per_layer_calls(ora):
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     kc2, vc2 = kc.clone(), vc.clone()
     out = da.decode_step_layers_fwd(q, kc, vc, kn, vn, p, max_kv_len_hint=cap, err_flag=err)
-    ref = torch.stack([da.decode_step_fwd(q[l], kc2[l], vc2[l], kn[l], vn[l], p, max_kv_len_hint=cap)
-                       for l in range(layers)])
+    flat = lambda t: t.reshape(layers * B, *t.shape[2:])  # noqa: E731
+    ref = da.decode_step_fwd(flat(q), flat(kc2), flat(vc2), flat(kn), flat(vn), p.repeat(layers),
+                             max_kv_len_hint=cap).view(q.shape)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
     assert torch.equal(kc.view(torch.int16), kc2.view(torch.int16))
     assert torch.equal(vc.view(torch.int16), vc2.view(torch.int16))
-    for l in (0, layers - 1):
+    for l in range(layers):
         kb, vb, o = oracle_step(ora, steps[l])
         assert np.array_equal(bits(kc[l]), kb) and np.array_equal(bits(vc[l]), vb)
         assert_close(out[l], o, f"layer {l}")
+
+
+def test_layers_call_rejects_before_any_write():
+    """An argument error of decode_step_layers_fwd (here a workspace sized for
+    one layer's batch, too small for the whole stack) is reported before the
+    launch: no layer's cache or output is touched."""
+    layers, B, H, Hkv, D, cap = 4, 1, 32, 8, 128, 20000
+    steps = [W.decode_step(B, H, Hkv, D, cap, "bf16", [19999], seed=70 + l) for l in range(layers)]
+    stack = lambda name: torch.stack([getattr(s, name) for s in steps]).cuda()  # noqa: E731
+    q, kc, vc, kn, vn = (stack(n) for n in ("q", "k_cache", "v_cache", "k_new", "v_new"))
+    p = steps[0].position_ids.cuda()
+    need_one = da.decode_attn_workspace_size(B, H, Hkv, D, cap)
+    need_all = da.decode_attn_workspace_size(layers * B, H, Hkv, D, cap)
+    small = torch.zeros(max(need_one, 16), dtype=torch.uint8, device="cuda")
+    kc0, vc0 = kc.clone(), vc.clone()
+    out = torch.full_like(q, 7.0)
+    if need_all > small.numel():
+        with pytest.raises(da.DecodeAttnError) as e:
+            da.decode_step_layers_fwd(q, kc, vc, kn, vn, p, out=out, workspace=small, max_kv_len_hint=cap)
+        assert e.value.status == -4
+    # a misaligned k_new (all layers share one alignment): rejected before the launch
+    lib = da.load_library()
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    st = lib.decode_step_layers_fwd(ptr(q), ptr(kc), ptr(vc), ctypes.c_void_p(kn.data_ptr() + 4), ptr(vn), ptr(p),
+                                    layers, B, H, Hkv, D, cap, 0.1, ptr(out), ptr(small), small.numel(), cap, 1,
+                                    None, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == -6
+    torch.cuda.synchronize()
+    assert torch.equal(kc.view(torch.int16), kc0.view(torch.int16))
+    assert torch.equal(vc.view(torch.int16), vc0.view(torch.int16))
+    assert bool((out.float() == 7.0).all())
 
 
 def test_binding_checks_flags_and_counts_workspace_bytes(ora):
