@@ -850,6 +850,105 @@ def run_reference(args) -> dict | None:
     }
 
 
+def run_case(args) -> dict:
+    """One named workload alone (for profiling one kernel instance): its CUDA
+    graph of public calls over rotating layer caches (>= 3x L2) replayed
+    `--warmup` then `--steps` times. Cases: long_context:<kv> (B=1, 32 / 8
+    heads, bf16, fused step), rope:<kv> (the same with rotary embedding),
+    mha:<kv> (B=1, 16 / 16 heads, fp16, fused step), batched (B=8, 16 / 8
+    heads, bf16, capacity 8192, ragged positions), s2pro_layers:<kv> (36
+    layers of 32 / 8 heads, bf16, capacity 32768, one decode_step_layers_fwd
+    launch per step)."""
+    import torch
+
+    import decode_attention_static_gb300 as da
+    import workloads as W
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    da.build_library()
+    da.load_library()
+    l2 = int(torch.cuda.get_device_properties(device).L2_cache_size)
+    name, _, arg = args.case.partition(":")
+    kv = int(arg) if arg else 8192
+    gen = torch.Generator(device="cpu").manual_seed(13)
+    if name in ("long_context", "rope", "mha"):
+        H, Hkv, dt = (16, 16, torch.float16) if name == "mha" else (32, 8, torch.bfloat16)
+        D = 128
+        layers = max(2, math.ceil(3 * l2 / (2 * Hkv * kv * D * 2)))
+        k = torch.empty(layers, 1, Hkv, kv, D, dtype=dt, device=device).normal_()
+        v = torch.empty_like(k).normal_()
+        q = torch.randn(layers, 1, H, D, generator=gen).to(dt).to(device)
+        kn = torch.randn(layers, 1, Hkv, D, generator=gen).to(dt).to(device)
+        vn = torch.randn(layers, 1, Hkv, D, generator=gen).to(dt).to(device)
+        out = torch.empty_like(q)
+        pos = torch.full((1,), kv - 1, dtype=torch.int32, device=device)
+        ws = da.alloc_workspace(1, H, Hkv, D, kv)
+        cos, sin = W.rope_tables(kv, D)
+        cos, sin = cos.to(device), sin.to(device)
+        calls = layers
+
+        def issue():
+            for l in range(layers):
+                if name == "rope":
+                    da.decode_step_rope_fwd(q[l], k[l], v[l], kn[l], vn[l], cos, sin, pos, out=out[l], workspace=ws,
+                                            max_kv_len_hint=kv)
+                else:
+                    da.decode_step_fwd(q[l], k[l], v[l], kn[l], vn[l], pos, out=out[l], workspace=ws,
+                                       max_kv_len_hint=kv)
+        nbytes = layers * (attend_bytes(1, H, Hkv, D, [kv], 2) + append_bytes(1, Hkv, D, 2))
+    elif name == "batched":
+        s0 = W.batched_streaming(seed=4)
+        hint = int(s0.position_ids.max()) + 1
+        kvs = (s0.position_ids + 1).tolist()
+        s0 = s0.to(device)
+        kc = [s0.k_cache] + [s0.k_cache.clone() for _ in range(2)]
+        vc = [s0.v_cache] + [s0.v_cache.clone() for _ in range(2)]
+        ws = da.alloc_workspace(s0.B, s0.n_head, s0.n_kv_head, s0.head_dim, s0.capacity)
+        calls = 6
+
+        def issue():
+            for i in range(calls):
+                da.decode_step_fwd(s0.q, kc[i % 3], vc[i % 3], s0.k_new, s0.v_new, s0.position_ids, workspace=ws,
+                                   max_kv_len_hint=hint)
+        nbytes = calls * (attend_bytes(s0.B, s0.n_head, s0.n_kv_head, s0.head_dim, kvs, 2)
+                          + append_bytes(s0.B, s0.n_kv_head, s0.head_dim, 2))
+    elif name == "s2pro_layers":
+        layers, H, Hkv, D, cap, dt = 36, 32, 8, 128, 32768, torch.bfloat16
+        k = torch.empty(layers, 1, Hkv, cap, D, dtype=dt, device=device).normal_()
+        v = torch.empty_like(k).normal_()
+        q = torch.randn(layers, 1, H, D, generator=gen).to(dt).to(device)
+        kn = torch.randn(layers, 1, Hkv, D, generator=gen).to(dt).to(device)
+        vn = torch.randn(layers, 1, Hkv, D, generator=gen).to(dt).to(device)
+        out = torch.empty_like(q)
+        pos = torch.full((1,), kv - 1, dtype=torch.int32, device=device)
+        ws = da.alloc_workspace(layers, H, Hkv, D, cap)
+        calls = 1
+
+        def issue():
+            da.decode_step_layers_fwd(q, k, v, kn, vn, pos, out=out, workspace=ws, max_kv_len_hint=kv)
+        nbytes = layers * (attend_bytes(1, H, Hkv, D, [kv], 2) + append_bytes(1, Hkv, D, 2))
+    else:
+        raise SystemExit(f"unknown case {args.case!r}")
+    issue()
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        issue()
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize(device)
+    ms = a.elapsed_time(b) / args.steps
+    return {"case": args.case, "calls_per_replay": calls, "us_per_call": round(ms * 1e3 / calls, 3),
+            "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "steps": args.steps, "warmup": args.warmup}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -869,9 +968,15 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the kv_len curve and the other configurations (reported beside the sweep)")
+    ap.add_argument("--case", default=None,
+                    help="run one named workload alone and print its timing (for profiling one kernel instance): "
+                         "long_context:<kv>, rope:<kv>, mha:<kv>, batched, s2pro_layers:<kv>")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.case:
+        print(json.dumps(run_case(args)), flush=True)
+        return
     res = run_reference(args) if args.impl == "reference" else run_ours(args)
     if res is not None:
         print(json.dumps(res), flush=True)
