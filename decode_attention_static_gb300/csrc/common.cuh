@@ -120,6 +120,18 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, 
       : "memory");
 }
 
+// The same without a cache hint.
+__device__ __forceinline__ void bulk_load_plain(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(smem_dst)),
+               "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+
+// Orders this thread's earlier generic-proxy view of global memory (for
+// instance data acquired from other CTAs) before its later bulk copies.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
 // Bulk prefetch of global memory into L2 (no completion tracking). Address
 // 16-byte aligned, bytes a positive multiple of 16.
 __device__ __forceinline__ void prefetch_l2(const void* gmem, uint32_t bytes) {

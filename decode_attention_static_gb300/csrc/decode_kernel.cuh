@@ -68,7 +68,7 @@ struct DecodeShape {
   // Layout after the ring: CTA state, receive area, then the mbarriers and
   // flags.
   static constexpr int kBarOffset = (kRingBytes + (kStateFloats + kRecvFloats) * 4 + 7) / 8 * 8;
-  static constexpr int kSmemBytes = kBarOffset + 2 * kStages * 8 + 16;
+  static constexpr int kSmemBytes = kBarOffset + (2 * kStages + 1) * 8 + 16;
   static constexpr int kPerThread = (G * D + kConsumerThreads - 1) / kConsumerThreads;
   static_assert(DPL == 8 || DPL == 16, "8 or 16 elements per lane");
   static_assert(G <= kLanesPerRow, "the score reduction gives each head its own lanes");
@@ -370,6 +370,78 @@ __device__ __forceinline__ void merge_partials(const DecodeParams& p, int64_t he
   }
 }
 
+// Partials merge_partials folds in one round trip to L2 (a batch of each
+// thread's share).
+template <int D, int G, int NT>
+__host__ __device__ constexpr int merge_one_trip() {
+  constexpr int E = G * D;
+  constexpr int R = E >= NT ? 1 : NT / E;
+  constexpr int KPT = R > 1 ? 1 : (E + NT - 1) / NT;
+  return (KPT >= 4 ? 8 : 16) * R;
+}
+
+// The same merge with the partials brought into shared memory first (when
+// there are more than merge_one_trip of them and the G x P partials fit
+// the idle ring): thread 0 copies each head's P
+// accumulator rows with one bulk copy while the threads load the (m, l)
+// pairs; the weights 2^(m_k - M) and the denominators are computed once per
+// (head, partial), and each output is then a P-term weighted sum read from
+// shared memory. One round trip to L2 whatever P is.
+template <typename T, int D, int G, int NT>
+__device__ __forceinline__ void merge_partials_smem(const DecodeParams& p, int64_t head0, int P, int nc,
+                                                    uint8_t* smem, uint64_t* bar) {
+  constexpr int E = G * D;
+  float* acc_s = reinterpret_cast<float*>(smem);  // [G][P][D]
+  float* ml_s = acc_s + G * P * D;                // [G][P][2]
+  float* w_s = ml_s + G * P * 2;                  // [G][P] weights, then [G] denominators
+  float* den_s = w_s + G * P;
+  if (threadIdx.x == 0) {
+    // The partials were written by other CTAs and acquired by this thread's
+    // arrival; the bulk copies read them through the async proxy.
+    fence_proxy_async_global();
+    mbar_arrive_expect_tx(bar, (uint32_t)(G * P * D * 4));
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      bulk_load_plain(acc_s + g * P * D, p.ws_acc + (head0 + g) * nc * D, (uint32_t)(P * D * 4), bar);
+  }
+  for (int t = threadIdx.x; t < G * P; t += NT) {
+    const int g = t / P, k = t - (t / P) * P;
+    const float* ml = p.ws_ml + ((head0 + g) * nc + k) * 2;
+    ml_s[2 * t] = __ldcg(ml);
+    ml_s[2 * t + 1] = __ldcg(ml + 1);
+  }
+  __syncthreads();
+  for (int t = threadIdx.x; t < G * P; t += NT) {
+    const int g = t / P;
+    float M = -INFINITY;
+    for (int k = 0; k < P; ++k) M = fmaxf(M, ml_s[2 * (g * P + k)]);
+    const float m = ml_s[2 * t];
+    w_s[t] = (m == -INFINITY) ? 0.f : fast_exp2(m - M);
+  }
+  __syncthreads();
+  if ((int)threadIdx.x < G) {
+    const int g = threadIdx.x;
+    float den = 0.f;
+    for (int k = 0; k < P; ++k) den = fmaf(ml_s[2 * (g * P + k) + 1], w_s[g * P + k], den);
+    den_s[g] = den;
+  }
+  const bool landed = mbar_wait(bar, 0);
+  __syncthreads();
+  if (!landed) {
+    if (threadIdx.x == 0 && p.err_flag) atomicOr(p.err_flag, kErrTimeout);
+    for (int i = threadIdx.x; i < E; i += NT) reinterpret_cast<uint16_t*>(p.out)[head0 * D + i] = Storage<T>::kNaN;
+    return;
+  }
+  for (int i = threadIdx.x; i < E; i += NT) {
+    const int g = i / D, d = i - (i / D) * D;
+    const float* a = acc_s + g * P * D + d;
+    const float* w = w_s + g * P;
+    float A = 0.f;
+    for (int k = 0; k < P; ++k) A = fmaf(w[k], a[k * D], A);
+    store_out<T>(p, head0 * D + i, A / den_s[g]);
+  }
+}
+
 template <typename T, int D, int G, int CW, int DPL, int NS, bool RP>
 __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const DecodeParams p) {
   using Shape = DecodeShape<D, G, CW, DPL, NS>;
@@ -386,7 +458,8 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
   float* recv = state + Shape::kStateFloats;   // receive area of the cluster merge
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Shape::kBarOffset);
   uint64_t* empty = full + kStages;
-  int* abort_flag = reinterpret_cast<int*>(empty + kStages);
+  uint64_t* merge_bar = empty + kStages;  // the partials' bulk copies of the workspace merge
+  int* abort_flag = reinterpret_cast<int*>(merge_bar + 1);
   int* last_flag = abort_flag + 1;
 
   const int s = blockIdx.x;
@@ -494,6 +567,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], CW);
     }
+    mbar_init(merge_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
     const int ch = chh;
@@ -943,7 +1017,12 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
     const int last = *reinterpret_cast<volatile int*>(last_flag);
     if (last > 0) {
       // the ring is idle now
-      merge_partials<T, D, G, Shape::kThreads>(p, head0, nclusters, p.splits / CS, reinterpret_cast<float*>(smem));
+      if (nclusters > merge_one_trip<D, G, Shape::kThreads>() &&
+          (int64_t)G * (nclusters * (D + 3) + 1) * 4 <= Shape::kRingBytes) {
+        merge_partials_smem<T, D, G, Shape::kThreads>(p, head0, nclusters, p.splits / CS, smem, merge_bar);
+      } else {
+        merge_partials<T, D, G, Shape::kThreads>(p, head0, nclusters, p.splits / CS, reinterpret_cast<float*>(smem));
+      }
     } else if (last < 0) {
       for (int i = threadIdx.x; i < E; i += Shape::kThreads)
         reinterpret_cast<uint16_t*>(p.out)[head0 * D + i] = S::kNaN;

@@ -56,3 +56,43 @@ def test_pipeline_timeout_is_reported_and_the_context_survives(ora, case):
     out2, err2 = _run(step, hint, ws)
     assert err2 == 0
     assert_close(out2, ref, f"{case}: after the timeout")
+
+
+def test_layers_call_timeout_is_reported_and_the_context_survives(ora):
+    """The same time-out inside the one-launch layers call: the hook leaves a
+    ring slot of layer 0's first KV head unfilled, so only that layer's query
+    heads of that KV head become NaN; every other layer and head is correct,
+    and the next layers call on the same workspace (zeroed again) is correct
+    everywhere."""
+    layers, B, H, Hkv, D, cap = 4, 1, 32, 8, 128, 1024
+    steps = [W.decode_step(B, H, Hkv, D, cap, "bf16", [634], seed=90 + l) for l in range(layers)]
+    G = H // Hkv
+    stack = lambda name: torch.stack([getattr(s, name) for s in steps]).cuda()  # noqa: E731
+
+    def run():
+        q, kc, vc, kn, vn = (stack(n) for n in ("q", "k_cache", "v_cache", "k_new", "v_new"))
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = da.decode_step_layers_fwd(q, kc, vc, kn, vn, steps[0].position_ids.cuda(), workspace=ws,
+                                        max_kv_len_hint=635, err_flag=err)
+        torch.cuda.synchronize()
+        return out, int(err.item())
+
+    ws = da.alloc_workspace(layers * B, H, Hkv, D, cap)
+    da.test_skip_slot(1)
+    try:
+        out, err = run()
+    finally:
+        da.test_skip_slot(-1)
+    assert err & DA_DEVERR_TIMEOUT, f"error flag {err}"
+    o = out.float()
+    assert bool(torch.isnan(o[0, 0, :G]).all()), "the timed-out group must be NaN"
+    assert bool(torch.isfinite(o[0, 0, G:]).all()) and bool(torch.isfinite(o[1:]).all()), "others unaffected"
+    refs = [oracle_step(ora, s)[2] for s in steps]
+    assert_close(out[0, :, G:], refs[0][:, G:], "layer 0, unaffected heads")
+    for l in range(1, layers):
+        assert_close(out[l], refs[l], f"layer {l}")
+    da.workspace_init(ws)
+    out2, err2 = run()
+    assert err2 == 0
+    for l in range(layers):
+        assert_close(out2[l], refs[l], f"layer {l} after the time-out")
