@@ -250,6 +250,83 @@ class SweepStep:
         return [i for i, (g, _) in enumerate(self.calls) if g == gi]
 
 
+def e2e_calls(torch, da, step, h_in, d_in, h_out, args, world, device, stream, mode: str) -> dict:
+    """The end-to-end step without a CUDA graph: per step one pinned H2D copy
+    of the inputs, every layer's public call issued from the host, one D2H
+    copy of the outputs. mode "c_abi" calls the C entry point through ctypes
+    with its arguments marshalled once (the host cost is the library's own:
+    validation, split plan, launch); "binding" calls the Python binding (which
+    also checks every tensor). Returns the time per step (ms) and the host
+    time per call (µs)."""
+    import ctypes
+
+    lib = da.load_library()
+    fused = step.fused
+    calls = []
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    vp = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    ws_bytes = step.workspace.numel()
+    for i, (g, layer) in enumerate(step.calls):
+        grp = step.groups[g]
+        q, kn, vn = step.inputs[i, 0], step.inputs[i, 1], step.inputs[i, 2]
+        kc, vc = grp["k"][layer], grp["v"][layer]
+        kv = grp["kv_len"]
+        if mode == "c_abi":
+            if fused:
+                calls.append((lib.decode_step_fwd, (vp(q), vp(kc), vp(vc), vp(kn), vp(vn), vp(step.positions[i]), B,
+                                                     N_HEAD, N_KV_HEAD, HEAD_DIM, kv, HEAD_DIM ** -0.5,
+                                                     vp(step.out[i]), vp(step.workspace), ws_bytes, kv, 0,
+                                                     vp(step.err), sptr)))
+            else:
+                calls.append((lib.kvcache_append, (vp(kc), vp(vc), vp(kn), vp(vn), vp(step.positions[i]), B,
+                                                    N_KV_HEAD, HEAD_DIM, kv, 0, vp(step.err), sptr)))
+                calls.append((lib.decode_attn_fwd, (vp(q), vp(kc), vp(vc), vp(step.kv_lens[i]), B, N_HEAD, N_KV_HEAD,
+                                                     HEAD_DIM, kv, HEAD_DIM ** -0.5, vp(step.out[i]),
+                                                     vp(step.workspace), ws_bytes, kv, 0, vp(step.err), sptr)))
+        else:
+            calls.append((i, q, kc, vc, kn, vn, kv))
+
+    def issue():
+        if mode == "c_abi":
+            for fn, a in calls:
+                if fn(*a) != 0:
+                    raise RuntimeError("decode call failed")
+        else:
+            for i, q, kc, vc, kn, vn, kv in calls:
+                if fused:
+                    da.decode_step_fwd(q, kc, vc, kn, vn, step.positions[i], out=step.out[i],
+                                       workspace=step.workspace, max_kv_len_hint=kv, err_flag=step.err)
+                else:
+                    da.kvcache_append(kc, vc, kn, vn, step.positions[i], err_flag=step.err)
+                    da.decode_attn_fwd(q, kc, vc, step.kv_lens[i], out=step.out[i], workspace=step.workspace,
+                                       max_kv_len_hint=kv, err_flag=step.err)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup // 4)):
+            d_in.copy_(h_in, non_blocking=True)
+            issue()
+            h_out.copy_(step.out, non_blocking=True)
+        barrier(world, device)
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        host_s = 0.0
+        wall0 = time.perf_counter()
+        e0.record(stream)
+        for _ in range(args.steps):
+            d_in.copy_(h_in, non_blocking=True)
+            t = time.perf_counter()
+            issue()
+            host_s += time.perf_counter() - t
+            h_out.copy_(step.out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        wall_ms = (time.perf_counter() - wall0) * 1e3
+    ms = max(e0.elapsed_time(e1), wall_ms)
+    ms_max = max_over_ranks(ms, world, device)
+    n_calls = len(calls) * (2 if (mode == "binding" and not fused) else 1)
+    return {"ms": ms_max, "host_us_per_call": round(host_s / (args.steps * n_calls) * 1e6, 2)}
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -352,18 +429,20 @@ def run_ours(args) -> dict | None:
     def replay_step():
         step_graph.replay()
 
-    for _ in range(args.warmup):
-        replay_step()
-    torch.cuda.synchronize(device)
-    if int(step.err.item()) != 0:
-        raise RuntimeError(f"device error flag {int(step.err.item())}")
-
     uuid = None
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
     except Exception:  # noqa: BLE001 - older torch: sample every GPU
         uuid = None
+    # sampled from the warm-up to the end of the last end-to-end leg (the
+    # timed region alone can be shorter than one sampling period)
     clocks = ClockSampler(uuid)
+
+    for _ in range(args.warmup):
+        replay_step()
+    torch.cuda.synchronize(device)
+    if int(step.err.item()) != 0:
+        raise RuntimeError(f"device error flag {int(step.err.item())}")
 
     # ---- timed region: exactly K steps ----
     stream = torch.cuda.current_stream(device)
@@ -465,6 +544,10 @@ def run_ours(args) -> dict | None:
     wall_ms = (time.perf_counter() - wall0) * 1e3
     e2e_ms = max(e0.elapsed_time(e1), wall_ms)
     e2e_ms_max = max_over_ranks(e2e_ms, world, device)
+
+    # ---- end to end without a graph: every layer's call made each step ----
+    direct = e2e_calls(torch, da, step, h_in, d_in, h_out, args, world, device, stream, mode="c_abi")
+    binding = e2e_calls(torch, da, step, h_in, d_in, h_out, args, world, device, stream, mode="binding")
     clk = clocks.stop()
     if int(step.err.item()) != 0:
         raise RuntimeError(f"device error flag {int(step.err.item())}")
@@ -532,6 +615,15 @@ def run_ours(args) -> dict | None:
                 "d2h_bytes_per_step": step.out.numel() * ELEM,
                 "mode": "one pinned H2D copy of every layer's q/k_new/v_new and positions, graph replay, one D2H "
                         "copy of the outputs"},
+        "e2e_direct": {"value": round(aggregate_value(bytes_step, args.steps, world, direct["ms"]), 1), "unit": UNIT,
+                       "h2d_bytes_per_step": step.h2d_bytes, "d2h_bytes_per_step": step.out.numel() * ELEM,
+                       "host_us_per_call": direct["host_us_per_call"],
+                       "mode": "no graph: one pinned H2D copy of the step's inputs, then every layer's call made "
+                               "through the C ABI (ctypes, arguments marshalled once), then one D2H copy of the "
+                               "outputs; wall clock and CUDA events, the larger"},
+        "e2e_binding": {"value": round(aggregate_value(bytes_step, args.steps, world, binding["ms"]), 1), "unit": UNIT,
+                        "host_us_per_call": binding["host_us_per_call"],
+                        "mode": "as e2e_direct, every call through the Python binding (tensor checks per call)"},
         "gpu_launches": step.launches_per_step() * args.steps,
         "clocks": clk,
     }
@@ -711,6 +803,7 @@ def other_configs(torch, da, device, l2_bytes: int) -> dict:
     vn = torch.randn(layers, 1, Hkv, D, generator=gen).to(dt).to(device)
     out = torch.empty_like(q)
     ws = da.alloc_workspace(1, H, Hkv, D, cap)
+    ws_layers = da.alloc_workspace(layers, H, Hkv, D, cap)
     gen_res = []
     for kv in (235, 435, 634):
         pos = torch.full((1,), kv - 1, dtype=torch.int32, device=device)
@@ -720,12 +813,21 @@ def other_configs(torch, da, device, l2_bytes: int) -> dict:
                 da.decode_step_fwd(q[l], k[l], v[l], kn[l], vn[l], pos, out=out[l], workspace=ws,
                                    max_kv_len_hint=kv)
 
+        def issue_layers():
+            da.decode_step_layers_fwd(q, k, v, kn, vn, pos, out=out, workspace=ws_layers, max_kv_len_hint=kv)
+
         warm = graph_us_per_call(torch, device, issue_s2, layers, 50)
         cold = graph_us_per_call(torch, device, issue_s2, layers, 20, flush=flush)
+        # every layer of the step in one launch (decode_step_layers_fwd), per layer-step
+        lw = graph_us_per_call(torch, device, issue_layers, 1, 200) / layers
+        lc = graph_us_per_call(torch, device, issue_layers, 1, 20, flush=flush) / layers
         b = attend_bytes(1, H, Hkv, D, [kv], 2) + append_bytes(1, Hkv, D, 2)
         gen_res.append({"kv_len": kv, "us_per_layer_step_as_run": round(warm, 3),
                         "us_per_layer_step_l2_flushed": round(cold, 3),
-                        "gbs_l2_flushed": round(b / (cold * 1e-6) / 1e9, 1)})
+                        "gbs_l2_flushed": round(b / (cold * 1e-6) / 1e9, 1),
+                        "layers_call_us_per_layer_step_as_run": round(lw, 3),
+                        "layers_call_us_per_layer_step_l2_flushed": round(lc, 3),
+                        "layers_call_gbs_l2_flushed": round(b / (lc * 1e-6) / 1e9, 1)})
     res["s2pro_generation"] = gen_res
     del k, v, flush_buf
     return res

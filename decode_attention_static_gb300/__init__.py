@@ -30,6 +30,7 @@ from ._binding import (  # noqa: F401
     prefix_ready,
     set_prefix_ready,
     set_timing_events,
+    shard_heads,
     splits_for,
     status_string,
     test_skip_slot,

@@ -58,6 +58,8 @@ _SIGNATURES = {
                          _i, _i, _vp, _vp], _i),
     "da_test_skip_slot": ([_i], _i),
     "da_set_prefix_ready": ([_i], _i),
+    "decode_attn_shard_heads": ([_i, _i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i), ctypes.POINTER(_i),
+                                 ctypes.POINTER(_i)], _i),
     "decode_step_layers_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _vp,
                                 ctypes.c_size_t, _i, _i, _vp, _vp], _i),
     "decode_step_rope_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _vp,
@@ -191,6 +193,15 @@ def splits_for(B: int, n_head: int, n_kv_head: int, head_dim: int, capacity: int
                                               _code_for(dtype), ctypes.byref(cs))
     _check("decode_attn_splits_for", s if s < 0 else 0)
     return s, cs.value
+
+
+def shard_heads(n_head: int, n_kv_head: int, world: int, rank: int) -> tuple[int, int, int, int]:
+    """(kv_head0, n_kv_local, head0, n_head_local) of rank `rank` in the
+    KV-head partition of decode_attn_shard_heads (host only)."""
+    out = [ctypes.c_int(0) for _ in range(4)]
+    st = load_library().decode_attn_shard_heads(n_head, n_kv_head, world, rank, *(ctypes.byref(o) for o in out))
+    _check("decode_attn_shard_heads", st)
+    return tuple(o.value for o in out)
 
 
 def set_timing_events(before: "torch.cuda.Event | None", after: "torch.cuda.Event | None") -> None:

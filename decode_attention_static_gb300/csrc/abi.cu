@@ -348,6 +348,22 @@ int decode_attn_splits_for(int B, int n_head, int n_kv_head, int head_dim, int c
   return splits;
 }
 
+int decode_attn_shard_heads(int n_head, int n_kv_head, int world, int rank, int* kv_head0, int* n_kv_local,
+                            int* head0, int* n_head_local) {
+  if (n_head < 1 || n_kv_head < 1 || n_head % n_kv_head != 0 || world < 1 || rank < 0 || rank >= world)
+    return DA_ERR_SHAPE;
+  if (!kv_head0 || !n_kv_local || !head0 || !n_head_local) return DA_ERR_NULL;
+  const int group = n_head / n_kv_head;
+  const int base = n_kv_head / world, extra = n_kv_head % world;
+  const int first = rank * base + std::min(rank, extra);
+  const int count = base + (rank < extra ? 1 : 0);
+  *kv_head0 = first;
+  *n_kv_local = count;
+  *head0 = first * group;
+  *n_head_local = count * group;
+  return DA_OK;
+}
+
 int da_test_skip_slot(int slot) {
   da::t_skip_slot = slot < 0 ? -1 : slot;
   return DA_OK;

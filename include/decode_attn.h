@@ -275,6 +275,26 @@ DA_API int decode_step_layers_fwd(const void* q, void* k_cache, void* v_cache, c
                     int n_kv_head, int head_dim, int capacity, float scale, void* out, void* workspace,
                     size_t workspace_bytes, int max_kv_len_hint, int dtype, int32_t* err_flag, void* stream);
 
+/*
+ * KV-head partition of one attention layer over `world` ranks (one GPU
+ * each), a pure host computation. Every (sequence, KV head) group is
+ * independent (its G = n_head / n_kv_head query heads read only that KV
+ * head), so rank r can own a contiguous block of KV heads with their query
+ * heads and run the decode calls of this header on its block alone, with no
+ * exchange of data: its caches are [B, n_kv_local, capacity, head_dim] for KV
+ * heads [kv_head0, kv_head0 + n_kv_local), its q and out [B, n_head_local,
+ * head_dim] for query heads [head0, head0 + n_head_local) (n_head_local =
+ * G * n_kv_local), and the ranks' outputs laid side by side on the head axis,
+ * in rank order, are the layer's output. KV heads are dealt as evenly as
+ * possible: the first n_kv_head % world ranks hold one more; a rank holds
+ * none when world > n_kv_head. (fish-speech issue #1310, section 2: the GQA
+ * head map h -> h / G; the pages run on one GPU, so this partition is this
+ * library's own.) Returns DA_OK, DA_ERR_SHAPE for inconsistent sizes or a
+ * rank outside [0, world), DA_ERR_NULL for a NULL output pointer.
+ */
+DA_API int decode_attn_shard_heads(int n_head, int n_kv_head, int world, int rank, int* kv_head0,
+                                   int* n_kv_local, int* head0, int* n_head_local);
+
 /* Size of the library-owned scratch array used by
  * decode_attn_fwd_static_scratch (1 MiB per GPU that loads the library). */
 #define DA_STATIC_SCRATCH_BYTES (1u << 20)

@@ -67,7 +67,7 @@ def _rank_main(rank, world, port, results):
 
 def test_two_rank_max_and_aggregate():
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         results = mgr.dict()
         mp.start_processes(_rank_main, args=(2, port, results), nprocs=2, join=True, start_method="spawn")
         r = dict(results)

@@ -373,3 +373,30 @@ def test_binding_checks_flags_and_counts_workspace_bytes(ora):
     torch.cuda.synchronize()
     assert np.array_equal(bits(d.k_cache), kb) and np.array_equal(bits(d.v_cache), vb)
     assert_close(out, ref, "float32 workspace")
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_kv_head_shards_concatenate_to_the_full_step(ora, world):
+    """Each rank's block of KV heads (decode_attn_shard_heads) run through the
+    fused step on its own contiguous tensors, one after another on this GPU:
+    the outputs side by side on the head axis, and the cache blocks, are the
+    full step's (outputs within tolerance: each block has its own split
+    plan), and match the oracle."""
+    step = W.decode_step(2, 32, 8, 128, 5000, "bf16", [4999, 2500], seed=85)
+    kb, vb, ref = oracle_step(ora, step)
+    outs, kcs, vcs = [], [], []
+    for rank in range(world):
+        kv0, nkv, h0, nh = da.shard_heads(step.n_head, step.n_kv_head, world, rank)
+        part = W.DecodeStep(step.q[:, h0:h0 + nh].contiguous(), step.k_cache[:, kv0:kv0 + nkv].contiguous(),
+                            step.v_cache[:, kv0:kv0 + nkv].contiguous(), step.k_new[:, kv0:kv0 + nkv].contiguous(),
+                            step.v_new[:, kv0:kv0 + nkv].contiguous(), step.position_ids, nh, nkv, step.dtype)
+        d, out, err = gpu_step(part, True, hint=5000)
+        assert err == 0
+        outs.append(out.cpu())
+        kcs.append(bits(d.k_cache))
+        vcs.append(bits(d.v_cache))
+    assert np.array_equal(np.concatenate(kcs, axis=1), kb) and np.array_equal(np.concatenate(vcs, axis=1), vb)
+    got = torch.cat(outs, dim=1)
+    assert_close(got, ref, f"{world} shards vs oracle")
+    _, full, _ = gpu_step(step, True, hint=5000)
+    assert_close(got, full.double().cpu().numpy(), f"{world} shards vs the full step")
