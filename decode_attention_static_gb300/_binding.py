@@ -117,21 +117,23 @@ def _dtype_code(t: torch.Tensor) -> int:
     return _code_for(t.dtype)
 
 
-def _require(cond: bool, msg: str) -> None:
+def _require(cond: bool, msg) -> None:
+    """Raise ValueError(msg) unless cond; msg may be a callable giving the
+    message (so that it is only formatted on failure)."""
     if not cond:
-        raise ValueError(msg)
+        raise ValueError(msg() if callable(msg) else msg)
 
 
 def _cuda_contig(name: str, t: torch.Tensor) -> None:
-    _require(t.is_cuda, f"{name} must be a CUDA tensor")
-    _require(t.is_contiguous(), f"{name} must be contiguous")
+    _require(t.is_cuda, lambda: f"{name} must be a CUDA tensor")
+    _require(t.is_contiguous(), lambda: f"{name} must be contiguous")
 
 
 def _on(device: torch.device, **tensors: torch.Tensor) -> None:
     """Every named tensor is a contiguous CUDA tensor on `device`."""
     for name, t in tensors.items():
         _cuda_contig(name, t)
-        _require(t.device == device, f"{name} is on {t.device}, the inputs on {device}")
+        _require(t.device == device, lambda: f"{name} is on {t.device}, the inputs on {device}")
 
 
 def _err_ptr(err_flag: torch.Tensor | None, device: torch.device):
@@ -151,8 +153,13 @@ def _workspace(workspace: torch.Tensor, device: torch.device):
 def _call(fn: str, device: torch.device, *args) -> None:
     """Call entry point `fn` with `device` current (the library launches on
     the current device, on the stream passed in `args`)."""
-    with torch.cuda.device(device):
-        st = getattr(load_library(), fn)(*args)
+    f = getattr(load_library(), fn)
+    index = device.index if device.index is not None else torch.cuda.current_device()
+    if torch.cuda.current_device() == index:
+        st = f(*args)
+    else:
+        with torch.cuda.device(device):
+            st = f(*args)
     _check(fn, st)
 
 

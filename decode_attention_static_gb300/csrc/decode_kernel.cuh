@@ -61,13 +61,11 @@ struct DecodeShape {
   static constexpr int kStageBytes = 2 * kTileBytes;                 // K tile then V tile
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kMergeFloats = CW * G * (D + 2);              // per-warp states (in the idle ring)
-  static constexpr int kStateFloats = G * D + 2 * G;                 // CTA state: acc[G][D], m[G], l[G]
   // Receive area of the cluster merge: (m, l) of up to kMaxCluster ranks and
   // their shares of this CTA's slice of the outputs (at most G*D + 15 floats).
   static constexpr int kRecvFloats = kMaxCluster * 2 * G + G * D + kMaxCluster;
-  // Layout after the ring: CTA state, receive area, then the mbarriers and
-  // flags.
-  static constexpr int kBarOffset = (kRingBytes + (kStateFloats + kRecvFloats) * 4 + 7) / 8 * 8;
+  // Layout after the ring: receive area, then the mbarriers and flags.
+  static constexpr int kBarOffset = (kRingBytes + kRecvFloats * 4 + 7) / 8 * 8;
   static constexpr int kSmemBytes = kBarOffset + (2 * kStages + 1) * 8 + 16;
   static constexpr int kPerThread = (G * D + kConsumerThreads - 1) / kConsumerThreads;
   static_assert(DPL == 8 || DPL == 16, "8 or 16 elements per lane");
@@ -454,8 +452,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
 
   extern __shared__ __align__(128) uint8_t smem[];
   float* red = reinterpret_cast<float*>(smem);  // per-warp states, once the ring is idle
-  float* state = reinterpret_cast<float*>(smem + Shape::kRingBytes);  // acc[G][D], m[G], l[G] of this CTA
-  float* recv = state + Shape::kStateFloats;   // receive area of the cluster merge
+  float* recv = reinterpret_cast<float*>(smem + Shape::kRingBytes);  // receive area of the cluster merge
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Shape::kBarOffset);
   uint64_t* empty = full + kStages;
   uint64_t* merge_bar = empty + kStages;  // the partials' bulk copies of the workspace merge
@@ -586,10 +583,12 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
       // gives each CTA a short chunk, one tile for chunks of at most two and
       // two for chunks of at most six (every CTA's first tiles then land
       // sooner and compete less with the previous kernel's streaming; the
-      // rest streams behind them), else a ring's worth.
-      const int ahead = (p.B == 1 && ch <= 2 * Shape::kTileRows)   ? 1
-                        : (p.B == 1 && ch <= 6 * Shape::kTileRows) ? min(2, kStages)
-                                                                   : kStages;
+      // rest streams behind them); two as well for the long chunks of the
+      // 4-stage instances (several query heads per KV head); else a ring's
+      // worth.
+      const int ahead = (p.B == 1 && ch <= 2 * Shape::kTileRows) ? 1
+                        : (p.B == 1 && (ch <= 6 * Shape::kTileRows || kStages == 4)) ? min(2, kStages)
+                                                                                    : kStages;
       const int rows = min(min(ch, lh - pr0), ahead * Shape::kTileRows);
       for (int t0 = 0; t0 < rows; t0 += Shape::kTileRows) {
         const int n = min(Shape::kTileRows, rows - t0);
@@ -700,6 +699,23 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
   const int per = (E + CS - 1) / CS;
   float* ml_in = recv;                 // [CS][2G]
   float* acc_in = recv + CS * 2 * G;   // [CS][per]
+
+  // Output i of the group, merged over this cluster: into `out` when one
+  // cluster holds the group, else as this cluster's partial in the workspace.
+  auto emit = [&](int i, float mm, float ls, float as) {
+    const int g = i / D;
+    const int d = i % D;
+    if (nclusters == 1) {
+      store_out<T>(p, head0 * D + i, as / ls);
+    } else {
+      const int64_t base = (head0 + g) * (p.splits / CS) + cid;
+      p.ws_acc[base * D + d] = as;
+      if (d == 0) {
+        p.ws_ml[base * 2] = mm;
+        p.ws_ml[base * 2 + 1] = ls;
+      }
+    }
+  };
 
   if (warp == CW) {
     // ---------------- producer warp ----------------
@@ -877,7 +893,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
     }
     asm volatile("bar.sync 1, %0;" ::"n"(CT) : "memory");
 
-    // Fold the warps into this CTA's state. A CTA whose pipeline timed out
+    // Fold the warps into one state per output. A CTA whose pipeline timed out
     // publishes NaN, which poisons every output of its group.
     const bool failed = *reinterpret_cast<volatile int*>(abort_flag) != 0;
     if (failed && threadIdx.x == 0 && p.err_flag) atomicOr(p.err_flag, kErrTimeout);
@@ -907,21 +923,14 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
         }
       }
     } else {
+      // A lone CTA: each folded output goes out (or into the workspace) at once.
 #pragma unroll
       for (int k = 0; k < Shape::kPerThread; ++k) {
         const int i = threadIdx.x + k * CT;
-        if (i < E) {
-          state[i] = failed ? nan : va[k];
-          if (i % D == 0) {
-            state[E + i / D] = failed ? nan : vm[k];
-            state[E + G + i / D] = vl[k];
-          }
-        }
+        if (i < E) emit(i, failed ? nan : vm[k], vl[k], failed ? nan : va[k]);
       }
     }
   }
-  // The cluster barrier below orders the pushes; a lone CTA reads its state.
-  if (CS == 1) __syncthreads();
 
   // ---------------- merge over the cluster ----------------
   // Rank k of the cluster merges outputs [k * per, (k + 1) * per). Every CTA
@@ -938,24 +947,9 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
     cluster_arrive_release();
     cluster_wait_acquire();
   }
-  auto emit = [&](int i, float mm, float ls, float as) {
-    const int g = i / D;
-    const int d = i % D;
-    if (nclusters == 1) {
-      store_out<T>(p, head0 * D + i, as / ls);
-    } else {
-      const int64_t base = (head0 + g) * (p.splits / CS) + cid;
-      p.ws_acc[base * D + d] = as;
-      if (d == 0) {
-        p.ws_ml[base * 2] = mm;
-        p.ws_ml[base * 2 + 1] = ls;
-      }
-    }
-  };
   constexpr int kLaneOutputs = 2 * (Shape::kThreads / 32);  // outputs per pass of the 16-lane merge
   if (CS == 1) {
-    for (int i = e0 + (int)threadIdx.x; i < e1; i += Shape::kThreads)
-      emit(i, state[E + i / D], state[E + G + i / D], state[i]);
+    // emitted by the fold above
   } else if (e1 - e0 > 2 * kLaneOutputs) {
     // A wide slice over few ranks: one thread per output, ranks in turn.
     for (int i = e0 + (int)threadIdx.x; i < e1; i += Shape::kThreads) {
