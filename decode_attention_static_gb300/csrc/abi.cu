@@ -215,9 +215,10 @@ int decode_common(const void* q, const void* k_cache, const void* v_cache, void*
   p.rope_rows = rope_rows;
   p.len_hint = bound;
   p.skip_slot = t_skip_slot;
-  // One sequence with an explicit bound: the bound is normally its length,
-  // so the kernel issues its first tiles before reading the length.
-  p.speculate = (B == 1 && max_kv_len_hint > 0) ? 1 : 0;
+  // One length (one sequence, or the layers of one sequence) with an explicit
+  // bound: the bound is normally that length, so the kernel issues its first
+  // tiles before reading the length.
+  p.speculate = (p.lens_period == 1 && max_kv_len_hint > 0) ? 1 : 0;
   p.prefix_ready = (p.speculate && t_prefix_ready) ? 1 : 0;
   p.qscale = scale * kLog2e;
   p.out = static_cast<uint8_t*>(out);
