@@ -577,9 +577,11 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
         const int rows = min(Shape::kTileRows, r1h - tr0);
         if (!(rope && tr0 + rows == lh)) issue(t, tr0, rows, lh, kSlotCached);
       }
-    } else if (pr0 < lh) {
-      // Pull the first tiles this CTA will probably read into L2, with rows
-      // from the host's length bound (clamped to the cache): when one sequence
+    } else if (pr0 < lh && p.speculate) {
+      // Pull the first tiles this CTA will read into L2, with rows from the
+      // host's length bound, when that bound is expected to be the length
+      // (one length and an explicit bound: otherwise rows past a sequence's
+      // prefix would be fetched from DRAM for nothing): when one sequence
       // gives each CTA a short chunk, one tile for chunks of at most two and
       // two for chunks of at most six (every CTA's first tiles then land
       // sooner and compete less with the previous kernel's streaming; the
