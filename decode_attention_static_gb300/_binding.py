@@ -107,6 +107,43 @@ def _stream(t: torch.Tensor) -> ctypes.c_void_p:
     return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
 
 
+# Fast accessors of torch's current device and raw current stream (plain
+# integers, no Python objects), with the public API as the fallback.
+_raw_stream_of = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_current_device_index = getattr(torch._C, "_cuda_getDevice", None)
+
+
+def _raw_stream(index: int) -> int:
+    if _raw_stream_of is not None:
+        return _raw_stream_of(index)
+    return torch.cuda.current_stream(index).cuda_stream
+
+
+def _device_now() -> int:
+    return _current_device_index() if _current_device_index is not None else torch.cuda.current_device()
+
+
+def _same_device_contiguous(index: int, names: tuple, tensors: tuple) -> None:
+    """Every tensor is a contiguous CUDA tensor on device `index` (one pass;
+    the detailed check runs only to name the offending tensor)."""
+    for name, t in zip(names, tensors):
+        if t.get_device() != index or not t.is_contiguous():
+            _on(torch.device("cuda", index), **{name: t})
+            raise ValueError(f"{name} must be a contiguous CUDA tensor on cuda:{index}")
+
+
+def _call_on(fn: str, index: int, *args) -> None:
+    """_call for a device given by index."""
+    f = getattr(load_library(), fn)
+    if _device_now() == index:
+        st = f(*args)
+    else:
+        with torch.cuda.device(index):
+            st = f(*args)
+    if st != 0:
+        _check(fn, st)
+
+
 def _code_for(dtype: torch.dtype) -> int:
     if dtype not in _DTYPE_CODE:
         raise TypeError(f"dtype {dtype} is not supported (float16 or bfloat16)")
@@ -254,18 +291,28 @@ def decode_attn_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
     """softmax(scale * q K[:kv_len]^T) V[:kv_len] per head; returns out [B, n_head, D]."""
     if out is None:
         out = torch.empty_like(q)
-    B, H, Hkv, D, cap = _attn_shapes(q, k_cache, v_cache, out)
-    dev = q.device
-    _on(dev, kv_len=kv_len)
+    _cuda_contig("q", q)
+    index = q.get_device()
+    _require(q.dim() == 3, "q must be [B, n_head, D]")
+    _require(k_cache.dim() == 4 and v_cache.shape == k_cache.shape, "caches must be [B, n_kv_head, capacity, D]")
+    B, H, D = q.shape
+    _, Hkv, cap, Dk = k_cache.shape
+    _require(k_cache.shape[0] == B and Dk == D, "cache batch/head_dim must match q")
+    _require(out.shape == q.shape, "out must be [B, n_head, D]")
+    _require(q.dtype == k_cache.dtype == v_cache.dtype == out.dtype, "dtypes differ")
     _require(kv_len.dtype == torch.int32 and kv_len.numel() == B, "kv_len must be int32 [B]")
-    if scale is None:
-        scale = D ** -0.5
     if workspace is None:
-        workspace = alloc_workspace(B, H, Hkv, D, cap, dev)
-    ws, ws_bytes = _workspace(workspace, dev)
-    _call("decode_attn_fwd", dev, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), B, H, Hkv, D, cap,
-          float(scale), _ptr(out), ws, ws_bytes, int(max_kv_len_hint), _dtype_code(q), _err_ptr(err_flag, dev),
-          _stream(q))
+        workspace = alloc_workspace(B, H, Hkv, D, cap, q.device)
+    names = ("k_cache", "v_cache", "out", "kv_len", "workspace")
+    tensors = (k_cache, v_cache, out, kv_len, workspace)
+    if err_flag is not None:
+        _require(err_flag.dtype == torch.int32 and err_flag.numel() >= 1, "err_flag must be int32 with one element")
+        names, tensors = names + ("err_flag",), tensors + (err_flag,)
+    _same_device_contiguous(index, names, tensors)
+    _call_on("decode_attn_fwd", index, q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), kv_len.data_ptr(), B, H,
+             Hkv, D, cap, float(D ** -0.5 if scale is None else scale), out.data_ptr(), workspace.data_ptr(),
+             workspace.numel() * workspace.element_size(), int(max_kv_len_hint), _code_for(q.dtype),
+             None if err_flag is None else err_flag.data_ptr(), _raw_stream(index))
     return out
 
 
@@ -290,16 +337,30 @@ def decode_step_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
     """Fused append at position_ids then attention over [0, position_ids]."""
     if out is None:
         out = torch.empty_like(q)
-    B, H, Hkv, D, cap = _step_inputs(q, k_cache, v_cache, k_new, v_new, position_ids, out)
-    dev = q.device
-    if scale is None:
-        scale = D ** -0.5
+    _cuda_contig("q", q)
+    index = q.get_device()
+    _require(q.dim() == 3, "q must be [B, n_head, D]")
+    _require(k_cache.dim() == 4 and v_cache.shape == k_cache.shape, "caches must be [B, n_kv_head, capacity, D]")
+    B, H, D = q.shape
+    _, Hkv, cap, Dk = k_cache.shape
+    _require(k_cache.shape[0] == B and Dk == D, "cache batch/head_dim must match q")
+    _require(out.shape == q.shape, "out must be [B, n_head, D]")
+    _require(k_new.shape == (B, Hkv, D) and v_new.shape == k_new.shape, "k_new/v_new must be [B, n_kv_head, D]")
+    _require(q.dtype == k_cache.dtype == v_cache.dtype == out.dtype == k_new.dtype == v_new.dtype, "dtypes differ")
+    _require(position_ids.dtype == torch.int32 and position_ids.numel() == B, "position_ids must be int32 [B]")
     if workspace is None:
-        workspace = alloc_workspace(B, H, Hkv, D, cap, dev)
-    ws, ws_bytes = _workspace(workspace, dev)
-    _call("decode_step_fwd", dev, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
-          _ptr(position_ids), B, H, Hkv, D, cap, float(scale), _ptr(out), ws, ws_bytes, int(max_kv_len_hint),
-          _dtype_code(q), _err_ptr(err_flag, dev), _stream(q))
+        workspace = alloc_workspace(B, H, Hkv, D, cap, q.device)
+    names = ("k_cache", "v_cache", "out", "k_new", "v_new", "position_ids", "workspace")
+    tensors = (k_cache, v_cache, out, k_new, v_new, position_ids, workspace)
+    if err_flag is not None:
+        _require(err_flag.dtype == torch.int32 and err_flag.numel() >= 1, "err_flag must be int32 with one element")
+        names, tensors = names + ("err_flag",), tensors + (err_flag,)
+    _same_device_contiguous(index, names, tensors)
+    _call_on("decode_step_fwd", index, q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), k_new.data_ptr(),
+             v_new.data_ptr(), position_ids.data_ptr(), B, H, Hkv, D, cap, float(D ** -0.5 if scale is None else scale),
+             out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+             int(max_kv_len_hint), _code_for(q.dtype), None if err_flag is None else err_flag.data_ptr(),
+             _raw_stream(index))
     return out
 
 
