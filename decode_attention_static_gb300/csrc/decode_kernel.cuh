@@ -908,19 +908,19 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
     const float nan = __int_as_float(0x7fc00000);
     if (CS > 1) {
       // Cluster plans: each folded value goes straight to the rank that
-      // merges it (distributed shared-memory stores), (m, l) to every rank.
+      // merges it (distributed shared-memory stores), (m, l) of each head to
+      // every rank: the thread folding column r of the head sends them to
+      // rank r (every thread of a head holds that head's m and l).
 #pragma unroll
       for (int k = 0; k < Shape::kPerThread; ++k) {
         const int i = threadIdx.x + k * CT;
         if (i < E) {
           const int kk = i / per;
           st_cluster_f32(acc_in + rank * per + (i - kk * per), kk, failed ? nan : va[k]);
-          if (i % D == 0) {
-            const int g = i / D;
-            for (int r = 0; r < CS; ++r) {
-              st_cluster_f32(ml_in + rank * 2 * G + g, r, failed ? nan : vm[k]);
-              st_cluster_f32(ml_in + rank * 2 * G + G + g, r, vl[k]);
-            }
+          const int g = i / D, r = i - g * D;
+          if (r < CS) {
+            st_cluster_f32(ml_in + rank * 2 * G + g, r, failed ? nan : vm[k]);
+            st_cluster_f32(ml_in + rank * 2 * G + G + g, r, vl[k]);
           }
         }
       }
