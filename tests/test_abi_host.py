@@ -191,6 +191,9 @@ def test_plain_c_program_uses_the_library(lib, tmp_path):
         "  int s = decode_attn_plan_splits(1, 16, 128, 8192, 152, 2, 16, &cs);\n"
         '  if (da_version() <= 0 || strcmp(da_status_string(DA_OK), "") == 0) return 1;\n'
         "  if (decode_attn_plan_splits(0, 16, 128, 8192, 152, 2, 16, &cs) != DA_ERR_SHAPE) return 2;\n"
+        "  int kv0, nkv, h0, nh;\n"
+        "  if (decode_attn_shard_heads(32, 8, 3, 2, &kv0, &nkv, &h0, &nh) != DA_OK) return 4;\n"
+        "  if (kv0 != 6 || nkv != 2 || h0 != 24 || nh != 8) return 5;\n"
         '  printf("%d %d\\n", s, cs);\n'
         "  return s >= 1 && cs >= 1 ? 0 : 3;\n}\n")
     exe = tmp_path / "consumer"
