@@ -23,6 +23,7 @@ from ._binding import (  # noqa: F401
     decode_step_layers_fwd,
     decode_step_rope_fwd,
     exported_symbols,
+    kernel_for,
     kvcache_append,
     library_path,
     load_library,

@@ -48,6 +48,7 @@ _SIGNATURES = {
     "decode_attn_workspace_size": ([_i, _i, _i, _i, _i], ctypes.c_size_t),
     "decode_attn_workspace_init": ([_vp, ctypes.c_size_t, _vp], _i),
     "decode_attn_splits_for": ([_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_i)], _i),
+    "decode_attn_kernel_for": ([_i, _i, _i, _i, _i, _i, _i, _i], _i),
     "da_set_timing_events": ([_vp, _vp], _i),
     "kvcache_append": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp], _i),
     "decode_attn_fwd": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _vp, ctypes.c_size_t, _i, _i,
@@ -237,6 +238,21 @@ def splits_for(B: int, n_head: int, n_kv_head: int, head_dim: int, capacity: int
                                               _code_for(dtype), ctypes.byref(cs))
     _check("decode_attn_splits_for", s if s < 0 else 0)
     return s, cs.value
+
+
+# decode_attn_kernel_for results
+KERNEL_NAMES = {0: "cuda_cores", 1: "tensor_cores", 2: "tensor_cores_paired"}
+
+
+def kernel_for(B: int, n_head: int, n_kv_head: int, head_dim: int, capacity: int, max_kv_len_hint: int = 0,
+               dtype: torch.dtype = torch.bfloat16, rotary: bool = False) -> str:
+    """The decode kernel a call with these sizes launches on the current device:
+    "cuda_cores", "tensor_cores" or "tensor_cores_paired" (for the layers call
+    pass layers * B as B)."""
+    k = load_library().decode_attn_kernel_for(B, n_head, n_kv_head, head_dim, capacity, int(max_kv_len_hint),
+                                              _code_for(dtype), 1 if rotary else 0)
+    _check("decode_attn_kernel_for", k if k < 0 else 0)
+    return KERNEL_NAMES[k]
 
 
 def shard_heads(n_head: int, n_kv_head: int, world: int, rank: int) -> tuple[int, int, int, int]:

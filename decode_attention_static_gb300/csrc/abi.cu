@@ -1,6 +1,7 @@
 // C ABI of the decode-attention library: argument validation, the split
 // plan, and the launches on the caller's stream. Nothing here allocates or
 // synchronises.
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 #include <algorithm>
@@ -19,8 +20,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct DeviceState {
   std::atomic<int> sms{0};
-  std::atomic<int> ready[4][2][4];  // [dtype + 2 * rotary][head_dim 64/128][log2 group]
-  DecodeKernelInfo info[4][2][4];
+  std::atomic<int> ready[4][2][4][3];  // [dtype + 2 * rotary][head_dim 64/128][log2 group][flavour]
+  DecodeKernelInfo info[4][2][4][3];
 };
 
 DeviceState g_devices[kMaxDevices];
@@ -70,42 +71,46 @@ bool decode_supported(int head_dim, int group) {
   return (head_dim == 64 || head_dim == 128) && (group == 1 || group == 2 || group == 4 || group == 8);
 }
 
-cudaError_t decode_kernel_info(int dtype, int head_dim, int group, int device, DecodeKernelInfo* info, bool rope) {
+cudaError_t decode_kernel_info(int dtype, int head_dim, int group, int device, DecodeKernelInfo* info, bool rope,
+                               int flavor) {
   const int ki = dtype + (rope ? 2 : 0);
   const int di = head_dim == 128 ? 1 : 0;
   const int gi = group_index(group);
+  const int ti = flavor >= 0 && flavor < 3 ? flavor : 0;
   DeviceState& st = g_devices[device];
-  if (st.ready[ki][di][gi].load(std::memory_order_acquire)) {
-    *info = st.info[ki][di][gi];
+  if (st.ready[ki][di][gi][ti].load(std::memory_order_acquire)) {
+    *info = st.info[ki][di][gi][ti];
     return cudaSuccess;
   }
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (!st.ready[ki][di][gi].load(std::memory_order_acquire)) {
+  if (!st.ready[ki][di][gi][ti].load(std::memory_order_acquire)) {
     DecodeKernelInfo k = {};
     cudaError_t e;
     if (rope) {
-      e = dtype == DA_F16 ? decode_info_f16_rope(head_dim, group, &k) : decode_info_bf16_rope(head_dim, group, &k);
+      e = dtype == DA_F16 ? decode_info_f16_rope(head_dim, group, ti, &k)
+                          : decode_info_bf16_rope(head_dim, group, ti, &k);
     } else {
-      e = dtype == DA_F16 ? decode_info_f16(head_dim, group, &k) : decode_info_bf16(head_dim, group, &k);
+      e = dtype == DA_F16 ? decode_info_f16(head_dim, group, ti, &k) : decode_info_bf16(head_dim, group, ti, &k);
     }
     if (e != cudaSuccess) return e;
     if (k.ctas_per_sm < 1) return cudaErrorInvalidConfiguration;
-    st.info[ki][di][gi] = k;
-    st.ready[ki][di][gi].store(1, std::memory_order_release);
+    st.info[ki][di][gi][ti] = k;
+    st.ready[ki][di][gi][ti].store(1, std::memory_order_release);
   }
-  *info = st.info[ki][di][gi];
+  *info = st.info[ki][di][gi][ti];
   return cudaSuccess;
 }
 
-cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int group, cudaStream_t stream) {
+cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int group, int flavor,
+                          cudaStream_t stream) {
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr.val.programmaticStreamSerializationAllowed = 1;
   if (p.rope_cos)
-    return dtype == DA_F16 ? launch_decode_f16_rope(p, head_dim, group, stream, &attr)
-                           : launch_decode_bf16_rope(p, head_dim, group, stream, &attr);
-  return dtype == DA_F16 ? launch_decode_f16(p, head_dim, group, stream, &attr)
-                         : launch_decode_bf16(p, head_dim, group, stream, &attr);
+    return dtype == DA_F16 ? launch_decode_f16_rope(p, head_dim, group, flavor, stream, &attr)
+                           : launch_decode_bf16_rope(p, head_dim, group, flavor, stream, &attr);
+  return dtype == DA_F16 ? launch_decode_f16(p, head_dim, group, flavor, stream, &attr)
+                         : launch_decode_bf16(p, head_dim, group, flavor, stream, &attr);
 }
 
 namespace {
@@ -126,9 +131,63 @@ cudaError_t record_event(cudaEvent_t ev, cudaStream_t st) {
   return cudaEventRecord(ev, st);
 }
 
-// Splits and cluster size for the current device: plan + occupancy of the instance.
+// cuTensorMapEncodeTiled of the driver, looked up once (null if unavailable).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult found = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &found) !=
+            cudaSuccess ||
+        found != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+static_assert(sizeof(TensorMap) == sizeof(CUtensorMap), "TensorMap holds a CUtensorMap");
+
+// The two K-cache tensor maps of the tensor-core instances: the cache as
+// [groups][capacity][head_dim] elements, boxes of 64 columns by one tile's
+// rows and by 8 rows, 128-byte swizzle, zero fill past the capacity.
+bool encode_k_maps(DecodeParams* p, const void* k_cache, int dtype, int64_t groups, int capacity, int head_dim) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)capacity, (cuuint64_t)groups};
+  const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)capacity * head_dim * 2};
+  const cuuint32_t box_tile[3] = {64, (cuuint32_t)tile_rows(head_dim), 1};
+  const cuuint32_t box_rows8[3] = {64, 8, 1};
+  const cuuint32_t unit[3] = {1, 1, 1};
+  const CUtensorMapDataType type = dtype == DA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  void* base = const_cast<void*>(k_cache);
+  if (enc(reinterpret_cast<CUtensorMap*>(&p->k_tiles), type, 3, base, dims, strides, box_tile, unit,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  return enc(reinterpret_cast<CUtensorMap*>(&p->k_rows8), type, 3, base, dims, strides, box_rows8, unit,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// CTAs that stream at most this many tiles each run the CUDA-core flavour of
+// the instances with four or more heads per KV head: its per-tile path is
+// shorter (no tensor-memory round trip), which wins until the tensor-core
+// flavour's higher streaming rate pays (measured, 32 / 8 heads, one
+// sequence: kv 256 / 1024 / 3072 / 6144 / 8192 at 1 / 2 / 4 / 8 / 7 tiles per
+// CTA take 4.22 / 5.27 / 7.02 / 9.74 / 11.1 us instead of 5.36 / 6.32 / 7.42
+// / 10.16 / 11.2; at kv 16384 and 32768, 14 and 27 tiles per CTA, the
+// tensor-core flavour takes 15.7 and 25.5 us instead of 16.5 and 26.2).
+constexpr int64_t kCudaCoreChunkTiles = 8;
+
+// Splits and cluster size for the current device: plan + occupancy of the
+// instance. *flavor (if given) gets the flavour of the instance the call
+// launches (rotary or not): the two-CTAs-per-SM one when the plan is one CTA
+// per group and the groups fill more than one wave of the one-per-SM kernel
+// (fewer waves), the CUDA-core one when each CTA streams few tiles, else the
+// default; *tensor_scores whether that kernel runs its scores on the tensor
+// cores (its K tiles then need tensor maps).
 int plan_for_device(int dtype, int B, int n_kv_head, int head_dim, int group, int bound, int* splits,
-                    int* cluster) {
+                    int* cluster, bool rope = false, bool* tensor_scores = nullptr, int* flavor = nullptr) {
   int device = 0, sms = 0;
   if (current_device(&device) != cudaSuccess) return DA_ERR_CUDA;
   if (device_sms(device, &sms) != cudaSuccess) return DA_ERR_CUDA;
@@ -138,6 +197,7 @@ int plan_for_device(int dtype, int B, int n_kv_head, int head_dim, int group, in
   DecodeKernelInfo info, info_rope;
   if (decode_kernel_info(dtype, head_dim, group, device, &info) != cudaSuccess) return DA_ERR_CUDA;
   if (decode_kernel_info(dtype, head_dim, group, device, &info_rope, true) != cudaSuccess) return DA_ERR_CUDA;
+  const bool default_tc = (rope ? info_rope.tensor_scores : info.tensor_scores) != 0;
   info.ctas_per_sm = std::min(info.ctas_per_sm, info_rope.ctas_per_sm);
   info.cluster_max = std::min(info.cluster_max, info_rope.cluster_max);
   for (int c = 0; c <= kMaxClusterSize; ++c)
@@ -156,6 +216,31 @@ int plan_for_device(int dtype, int B, int n_kv_head, int head_dim, int group, in
   if (s < 1) return s;
   *splits = s;
   *cluster = cs;
+  int f = kFlavorWide;
+  if (default_tc) {
+    if (s == 1 && units > (int64_t)sms * info.ctas_per_sm) {
+      // The occupancy query reports one CTA per SM for the pair flavour as
+      // well, but two run at once (measured: the 288-group S2-Pro layers call
+      // takes 20.5 us instead of 24.6 at kv 634); a plan of one CTA per group
+      // never depends on CTAs being co-resident.
+      DecodeKernelInfo pair;
+      if (decode_kernel_info(dtype, head_dim, group, device, &pair, rope, kFlavorPair) != cudaSuccess)
+        return DA_ERR_CUDA;
+      if (pair.flavor == kFlavorPair) f = kFlavorPair;
+    } else {
+      const int64_t rows = tile_rows(head_dim);
+      const int64_t tiles = ((int64_t)bound + rows - 1) / rows;
+      if ((tiles + s - 1) / s <= kCudaCoreChunkTiles) {
+        // Only where the same clusters fit that kernel too.
+        DecodeKernelInfo cc;
+        if (decode_kernel_info(dtype, head_dim, group, device, &cc, rope, kFlavorCudaCores) != cudaSuccess)
+          return DA_ERR_CUDA;
+        if (cc.flavor == kFlavorCudaCores && (cs == 1 || cc.active_clusters[cs] >= units)) f = kFlavorCudaCores;
+      }
+    }
+  }
+  if (flavor) *flavor = f;
+  if (tensor_scores) *tensor_scores = default_tc && f != kFlavorCudaCores;
   return DA_OK;
 }
 
@@ -185,7 +270,10 @@ int decode_common(const void* q, const void* k_cache, const void* v_cache, void*
   const int group = n_head / n_kv_head;
   const int bound = max_kv_len_hint > 0 ? std::min(max_kv_len_hint, capacity) : capacity;
   int splits = 1, cluster = 1;
-  rc = plan_for_device(dtype, B, n_kv_head, head_dim, group, bound, &splits, &cluster);
+  bool tensor_scores = false;
+  int flavor = 0;
+  rc = plan_for_device(dtype, B, n_kv_head, head_dim, group, bound, &splits, &cluster, rope_cos != nullptr,
+                       &tensor_scores, &flavor);
   if (rc != DA_OK) return rc;
   const size_t need = workspace_bytes_for(B, n_head, splits, cluster, head_dim);
   if (need > 0) {
@@ -229,10 +317,12 @@ int decode_common(const void* q, const void* k_cache, const void* v_cache, void*
     p.ws_ml = p.ws_acc + (size_t)B * n_head * (splits / cluster) * head_dim;
   }
   p.err_flag = err_flag;
+  if (tensor_scores && !encode_k_maps(&p, k_cache, dtype, (int64_t)B * n_kv_head, capacity, head_dim))
+    return DA_ERR_CUDA;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (t_event_before && record_event(t_event_before, st) != cudaSuccess) return DA_ERR_CUDA;
-  if (launch_decode(p, dtype, head_dim, group, st) != cudaSuccess) return DA_ERR_CUDA;
+  if (launch_decode(p, dtype, head_dim, group, flavor, st) != cudaSuccess) return DA_ERR_CUDA;
   if (t_event_after && record_event(t_event_after, st) != cudaSuccess) return DA_ERR_CUDA;
   return DA_OK;
 }
@@ -286,7 +376,12 @@ int decode_attn_plan_splits(int B, int n_kv_head, int head_dim, int max_kv_len, 
       // CTAs: no split at all.
       const int64_t c = std::min<int64_t>(
           {fit, std::max<int64_t>(1, num_sms / units), (tiles + ctas_per_sm - 1) / ctas_per_sm});
-      if (tiles <= da::kClusterTilesPerSplit * std::max<int64_t>(c, 1)) cs = c >= 2 ? c : 0;
+      // A CTA alone on its SM streams about twice the tiles in the time its
+      // cluster merge saves over the workspace merge (measured with four
+      // query heads per KV head: clusters of 12 beat 19 flat splits up to
+      // 96 tiles), so the bound doubles at one CTA per SM.
+      const int64_t per_split = ctas_per_sm == 1 ? 2 * da::kClusterTilesPerSplit : da::kClusterTilesPerSplit;
+      if (tiles <= per_split * std::max<int64_t>(c, 1)) cs = c >= 2 ? c : 0;
     }
     if (cs > 1) {
       want = cs;
@@ -347,6 +442,21 @@ int decode_attn_splits_for(int B, int n_head, int n_kv_head, int head_dim, int c
   }
   if (cluster_size) *cluster_size = cluster;
   return splits;
+}
+
+int decode_attn_kernel_for(int B, int n_head, int n_kv_head, int head_dim, int capacity, int max_kv_len_hint,
+                           int dtype, int rotary) {
+  int rc = da::check_sizes(B, n_head, n_kv_head, head_dim, capacity, dtype);
+  if (rc != DA_OK) return rc;
+  if (B == 0) return DA_KERNEL_CUDA_CORES;
+  const int bound = max_kv_len_hint > 0 ? std::min(max_kv_len_hint, capacity) : capacity;
+  int splits = 1, cluster = 1, flavor = 0;
+  bool tensor_scores = false;
+  rc = da::plan_for_device(dtype, B, n_kv_head, head_dim, n_head / n_kv_head, bound, &splits, &cluster, rotary != 0,
+                           &tensor_scores, &flavor);
+  if (rc != DA_OK) return rc;
+  if (!tensor_scores) return DA_KERNEL_CUDA_CORES;
+  return flavor == da::kFlavorPair ? DA_KERNEL_TENSOR_CORES_PAIRED : DA_KERNEL_TENSOR_CORES;
 }
 
 int decode_attn_shard_heads(int n_head, int n_kv_head, int world, int rank, int* kv_head0, int* n_kv_local,

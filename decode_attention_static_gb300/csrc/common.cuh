@@ -27,10 +27,17 @@ constexpr int kTileBytes = 16384;
 constexpr int kMaxSplits = 128;
 // Largest thread-block cluster of split CTAs (the non-portable hardware limit).
 constexpr int kMaxClusterSize = 16;
-// A group whose splits would stream at most this many tiles each is served
-// by one thread-block cluster (on-chip merge); longer prefixes are split
-// over every resident CTA and merged through the workspace.
+// A group whose splits would stream at most this many tiles each (twice as
+// many for instances that run one CTA per SM) is served by one thread-block
+// cluster (on-chip merge); longer prefixes are split over every resident CTA
+// and merged through the workspace.
 constexpr int kClusterTilesPerSplit = 4;
+// Kernel flavours of the instances with four or more query heads per KV
+// head (InstanceConfig in decode_kernel.cuh): tensor-core scores with one CTA
+// per SM, the same with two CTAs per SM, and CUDA-core scores.
+constexpr int kFlavorWide = 0;
+constexpr int kFlavorPair = 1;
+constexpr int kFlavorCudaCores = 2;
 // The workspace starts with one 32-bit arrival counter per (sequence, KV
 // head) group, in a fixed region so that calls of any shape find their
 // counters at the same place; split decoding is used only for at most
@@ -156,6 +163,123 @@ __device__ __forceinline__ void st_cluster_f32(float* local, int rank, float v) 
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
+// ---------------------------------------------------------------------------
+// Tensor-memory scores (fifth-generation tensor cores, sm_100 family).
+//
+// The score tile S^T = K q^T of the instances with several query heads per
+// KV head runs as tcgen05.mma (kind::f16: fp16 or bf16 operands, fp32
+// accumulation) with the K tile (A, M = 128 rows) and the q operand (B,
+// N = 16 rows: the group's heads, the rest zero) in shared memory, both
+// K-major with the 128-byte swizzle that TMA tensor copies write, and the
+// accumulator in tensor memory (row i of S^T in lane i).
+
+// Opaque copy of a CUtensorMap (a 128-byte, 64-byte aligned descriptor that
+// the host encodes with cuTensorMapEncodeTiled).
+struct alignas(64) TensorMap {
+  unsigned long long words[16];
+};
+
+// 3-D tiled TMA copy global -> shared: the box at element coordinates
+// (x, y, z) of `map`, completing on `bar`. x * element size must be a
+// multiple of 16 bytes.
+__device__ __forceinline__ void tensor_load_3d(void* smem_dst, const TensorMap* map, int x, int y, int z,
+                                               uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(smem_dst)),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy reads of them (the tensor core reading an operand).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Tensor-memory allocation of `cols` columns (a power of two >= 32) by one
+// whole warp; the base address is written to *slot.
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(slot)), "r"(cols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_free(uint32_t base, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(cols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte
+// swizzle layout: 8-row atoms of 128-byte rows, 1024 bytes apart (stride
+// byte offset); the leading byte offset is unused in this layout.
+__device__ __forceinline__ uint64_t sw128_desc(const void* smem_ptr) {
+  const uint32_t a = smem_addr(smem_ptr);
+  return (uint64_t)((a & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
+         (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16 with fp32 accumulation, both operands
+// K-major, M = 128 and N = 16; `bf16` selects bf16 operands (else fp16).
+__host__ __device__ constexpr uint32_t mma_idesc_m128_n16(bool bf16) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
+}
+
+// D (tensor memory) = A B^T (+ D when `accumulate`), issued by one thread.
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred acc;\n\tsetp.ne.b32 acc, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, acc;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05.mma this thread issued before has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+// This warp's 32 lanes of tensor memory (the lanes of its subpartition),
+// N consecutive 32-bit columns from `taddr`, then wait for the load.
+template <int N>
+__device__ __forceinline__ void tmem_load(uint32_t taddr, uint32_t (&r)[N]) {
+  static_assert(N == 4 || N == 8, "4 or 8 columns");
+  if constexpr (N == 4) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr)
+                 : "memory");
+  } else {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
+  }
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Named barrier ID over COUNT threads (whole warps).
+template <int ID, int COUNT>
+__device__ __forceinline__ void named_barrier_sync() {
+  asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(COUNT) : "memory");
+}
+
+// Named barrier ID over COUNT threads that also returns whether any of them
+// passed true.
+template <int ID, int COUNT>
+__device__ __forceinline__ bool named_barrier_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, %2, %3, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "n"(ID), "n"(COUNT)
+      : "memory");
+  return r != 0;
+}
+
 // Programmatic dependent launch: wait for the preceding grid's memory, and
 // allow the following grid to be scheduled.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -222,6 +346,7 @@ struct Storage<__nv_bfloat16> {
   }
   static __device__ __forceinline__ uint16_t round(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
   static constexpr uint16_t kNaN = 0x7FC0;
+  static constexpr bool kBf16 = true;
 };
 
 template <>
@@ -252,6 +377,7 @@ struct Storage<__half> {
   }
   static __device__ __forceinline__ uint16_t round(float x) { return __half_as_ushort(__float2half_rn(x)); }
   static constexpr uint16_t kNaN = 0x7E00;
+  static constexpr bool kBf16 = false;
 };
 
 // Rotary position embedding of one 16-byte vector x (8 elements at columns
@@ -307,7 +433,13 @@ __device__ __forceinline__ void load_f32x8(const float* table, int64_t row, int 
 }
 
 // Parameters of one decode-kernel launch.
-struct DecodeParams {
+struct alignas(64) DecodeParams {
+  // Instances with tensor-memory scores: the K cache as a 3-D tensor
+  // [B * n_kv_head][capacity][D] with a box of one tile's rows (k_tiles) and
+  // of 8 rows (k_rows8, for the last partial tile), 64 columns wide, 128-byte
+  // swizzle. Unused by the other instances.
+  TensorMap k_tiles;
+  TensorMap k_rows8;
   const uint8_t* q;        // [B, n_head, D]
   const uint8_t* k_cache;  // [B, n_kv_head, capacity, D]
   const uint8_t* v_cache;

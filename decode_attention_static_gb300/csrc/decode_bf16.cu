@@ -3,12 +3,12 @@
 
 namespace da {
 
-cudaError_t launch_decode_bf16(const DecodeParams& p, int head_dim, int group, cudaStream_t stream,
+cudaError_t launch_decode_bf16(const DecodeParams& p, int head_dim, int group, int flavor, cudaStream_t stream,
                               const cudaLaunchAttribute* attr) {
   DA_DISPATCH(__nv_bfloat16, false, launch_decode_t, p, stream, attr)
 }
 
-cudaError_t decode_info_bf16(int head_dim, int group, DecodeKernelInfo* info) {
+cudaError_t decode_info_bf16(int head_dim, int group, int flavor, DecodeKernelInfo* info) {
   DA_DISPATCH(__nv_bfloat16, false, decode_info_t, info)
 }
 

@@ -1,6 +1,8 @@
 // Instantiation and launch of the decode kernel for one storage type over
 // head_dim in {64, 128} and group size in {1, 2, 4, 8}; RP selects the
-// instances of the fused step with rotary embedding.
+// instances of the fused step with rotary embedding, `flavor` one of the
+// InstanceConfig flavours (distinct kernels for four or more heads per KV
+// head only).
 #pragma once
 
 #include "decode_kernel.cuh"
@@ -8,19 +10,20 @@
 
 namespace da {
 
-template <int D, int G>
+template <int D, int G, int F>
 using ConfiguredShape = DecodeShape<D, G, DecodeConfig<D, G>::kWarps, DecodeConfig<D, G>::kPerLane,
-                                    DecodeConfig<D, G>::kStages>;
+                                    InstanceConfig<D, G, F>::kStages, InstanceConfig<D, G, F>::kTensorScores>;
 
-template <typename T, int D, int G, bool RP>
+template <typename T, int D, int G, bool RP, int F>
 constexpr auto configured_kernel() {
-  return decode_split_kernel<T, D, G, DecodeConfig<D, G>::kWarps, DecodeConfig<D, G>::kPerLane,
-                             DecodeConfig<D, G>::kStages, RP>;
+  using C = InstanceConfig<D, G, F>;
+  return decode_split_kernel<T, D, G, DecodeConfig<D, G>::kWarps, DecodeConfig<D, G>::kPerLane, C::kStages, RP,
+                             C::kTensorScores, C::kMinBlocks>;
 }
 
-template <typename T, int D, int G, bool RP>
+template <typename T, int D, int G, bool RP, int F>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream, const cudaLaunchAttribute* pdl) {
-  using Shape = ConfiguredShape<D, G>;
+  using Shape = ConfiguredShape<D, G, F>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.splits, p.n_kv_head, p.B);
   cfg.blockDim = dim3(Shape::kThreads);
@@ -38,17 +41,17 @@ cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream, const cu
   }
   cfg.attrs = attrs;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, configured_kernel<T, D, G, RP>(), p);
+  return cudaLaunchKernelEx(&cfg, configured_kernel<T, D, G, RP, F>(), p);
 }
 
 // Applies the shared-memory and cluster-size opt-ins for the current device
 // and reports the occupancy of one instance: resident CTAs per SM and the
 // largest cluster (16, else 8) of which at least one fits.
-template <typename T, int D, int G, bool RP>
+template <typename T, int D, int G, bool RP, int F>
 cudaError_t decode_info_t(DecodeKernelInfo* info) {
-  using Shape = ConfiguredShape<D, G>;
+  using Shape = ConfiguredShape<D, G, F>;
   const int smem = Shape::kSmemBytes;
-  auto* fn = configured_kernel<T, D, G, RP>();
+  auto* fn = configured_kernel<T, D, G, RP, F>();
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -58,6 +61,8 @@ cudaError_t decode_info_t(DecodeKernelInfo* info) {
   if (e != cudaSuccess) return e;
   info->smem_bytes = smem;
   info->ctas_per_sm = n;
+  info->tensor_scores = InstanceConfig<D, G, F>::kTensorScores ? 1 : 0;
+  info->flavor = InstanceConfig<D, G, F>::kFlavor;
   info->cluster_max = 1;
   for (int cs = 16; cs >= 1; --cs) {
     cudaLaunchConfig_t cfg = {};
@@ -82,13 +87,20 @@ cudaError_t decode_info_t(DecodeKernelInfo* info) {
   return cudaSuccess;
 }
 
-#define DA_DISPATCH_GROUP(T, RP, D, FN, ...)             \
-  switch (group) {                                       \
-    case 1: return FN<T, D, 1, RP>(__VA_ARGS__);         \
-    case 2: return FN<T, D, 2, RP>(__VA_ARGS__);         \
-    case 4: return FN<T, D, 4, RP>(__VA_ARGS__);         \
-    case 8: return FN<T, D, 8, RP>(__VA_ARGS__);         \
-    default: return cudaErrorInvalidValue;               \
+#define DA_DISPATCH_FLAVOR(T, RP, D, G, FN, ...)                   \
+  switch (flavor) {                                                \
+    case kFlavorPair: return FN<T, D, G, RP, kFlavorPair>(__VA_ARGS__);        \
+    case kFlavorCudaCores: return FN<T, D, G, RP, kFlavorCudaCores>(__VA_ARGS__); \
+    default: return FN<T, D, G, RP, kFlavorWide>(__VA_ARGS__);                 \
+  }
+
+#define DA_DISPATCH_GROUP(T, RP, D, FN, ...)                          \
+  switch (group) {                                                    \
+    case 1: return FN<T, D, 1, RP, kFlavorWide>(__VA_ARGS__);         \
+    case 2: return FN<T, D, 2, RP, kFlavorWide>(__VA_ARGS__);         \
+    case 4: DA_DISPATCH_FLAVOR(T, RP, D, 4, FN, __VA_ARGS__)          \
+    case 8: DA_DISPATCH_FLAVOR(T, RP, D, 8, FN, __VA_ARGS__)          \
+    default: return cudaErrorInvalidValue;                            \
   }
 
 #define DA_DISPATCH(T, RP, FN, ...)                                         \

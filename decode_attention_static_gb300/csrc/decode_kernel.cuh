@@ -41,12 +41,17 @@ namespace da {
 // cluster sizes).
 constexpr int kMaxCluster = 16;
 
-template <int D, int G, int CW, int DPL, int NS>
+template <int D, int G, int CW, int DPL, int NS, bool TC = false>
 struct DecodeShape {
   static constexpr int kStages = NS;                                 // depth of the shared-memory ring
   static constexpr int kConsumerWarps = CW;
   static constexpr int kConsumerThreads = CW * 32;
-  static constexpr int kThreads = kConsumerThreads + 32;             // + the producer warp
+  // + the producer warp (+ the warp issuing the tensor-core scores)
+  static constexpr int kThreads = kConsumerThreads + (TC ? 64 : 32);
+  // Warps that release a ring stage once they are done with it: every
+  // consumer warp, or with tensor-core scores the four warps of the group
+  // that consumed the tile.
+  static constexpr int kEmptyArrivals = TC ? 4 : CW;
   static constexpr int kRowBytes = 2 * D;
   static constexpr int kTileRows = kTileBytes / kRowBytes;           // 64 for D=128, 128 for D=64
   static constexpr int kVecs = DPL / 8;                              // 16-byte vectors per lane per row
@@ -64,9 +69,31 @@ struct DecodeShape {
   // Receive area of the cluster merge: (m, l) of up to kMaxCluster ranks and
   // their shares of this CTA's slice of the outputs (at most G*D + 15 floats).
   static constexpr int kRecvFloats = kMaxCluster * 2 * G + G * D + kMaxCluster;
-  // Layout after the ring: receive area, then the mbarriers and flags.
-  static constexpr int kBarOffset = (kRingBytes + kRecvFloats * 4 + 7) / 8 * 8;
-  static constexpr int kSmemBytes = kBarOffset + (2 * kStages + 1) * 8 + 16;
+  // Tensor-core scores: the q operand (16 rows of D elements as 64-column
+  // halves of 128-byte swizzled rows, 1024-byte aligned), the weights of the
+  // two consumer groups' current tiles [2][kTileRows][G], and small
+  // per-group arrays: tile maxima [2][4][G], weight sums
+  // [2][4][G], running maxima [2][G], the new row's scores [G] and the
+  // tensor-memory base address.
+  static constexpr int kQOffset = (kRingBytes + kRecvFloats * 4 + 1023) / 1024 * 1024;
+  static constexpr int kQBytes = 16 * 2 * D;
+  static constexpr int kPOffset = kQOffset + kQBytes;
+  static constexpr int kAuxOffset = kPOffset + 2 * kTileRows * G * 4;
+  static constexpr int kAuxFloats = 8 * G + 8 * G + 2 * G + G + 1;
+  // Layout after the ring: receive area, (tensor-core extras,) then the
+  // mbarriers (full, empty, merge, and with tensor-core scores two
+  // score-ready and two score-free) and flags.
+  static constexpr int kBarOffset =
+      TC ? (kAuxOffset + kAuxFloats * 4 + 7) / 8 * 8 : (kRingBytes + kRecvFloats * 4 + 7) / 8 * 8;
+  static constexpr int kBars = 2 * kStages + 1 + (TC ? 4 : 0);
+  // (+ 1024 bytes of slack for aligning the ring to the 128-byte swizzle atoms)
+  static constexpr int kSmemBytes = kBarOffset + kBars * 8 + 16 + (TC ? 1024 : 0);
+  // Tensor-core weighted sum of V: a row is read by D/8 threads (16 bytes
+  // each); the 128 threads of a group form 128 / (D/8) row groups of
+  // kTileRows / (128 / (D/8)) rows each.
+  static constexpr int kVThreadsPerRow = D / 8;
+  static constexpr int kRowGroups = 128 / kVThreadsPerRow;
+  static constexpr int kRowsPerThread = kTileRows / kRowGroups;
   static constexpr int kPerThread = (G * D + kConsumerThreads - 1) / kConsumerThreads;
   static_assert(DPL == 8 || DPL == 16, "8 or 16 elements per lane");
   static_assert(G <= kLanesPerRow, "the score reduction gives each head its own lanes");
@@ -75,23 +102,54 @@ struct DecodeShape {
   static_assert(kBarOffset % 8 == 0, "mbarriers need 8-byte alignment");
   static_assert(kVecs == 1, "one 16-byte vector per lane (rotary embedding pairs lanes c and c ^ D/16)");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
+  static_assert(!TC || (CW == 8 && G <= 16 && D % 64 == 0 && kTileRows % 32 == 0 && kTileRows <= 128),
+                "tensor-core scores: two groups of four consumer warps, at most 16 heads, whole 64-column halves");
+  static_assert(!TC || kRowsPerThread * kRowGroups == kTileRows, "V rows split evenly over the row groups");
+  static_assert(!TC || 2 * kRowGroups * G * D * 4 <= kRingBytes, "the group partials fit the ring");
 };
 
-// Consumer warps, elements per lane and ring depth of each instance. Scores
-// take one mixed-precision FMA per element and head on the raw 16-bit q and
-// K (packed fp32x2 products on converted K measured no faster). A 3-stage ring of 32 KiB stages (96 KiB) per CTA covers the
-// loaded HBM latency and leaves room for two CTAs per SM: thread-block
-// clusters of up to 13 CTAs then fit once per group for 16 groups, and the
-// next launch's CTAs can be resident while this one drains. G >= 4 needs too
-// many registers for two CTAs per SM anyway and takes a 4-stage ring (more
-// bytes in flight for its long flat splits; 6 stages measured slower). Eight elements
-// per lane (one 16-byte vector of a row) give each warp more independent rows
-// per tile than sixteen, and fewer registers for the G query slices.
+// Consumer warps, elements per lane and ring depth of each instance. With
+// one or two query heads per KV head, scores take one mixed-precision FMA
+// per element and head on the raw 16-bit q and K (packed fp32x2 products on
+// converted K measured no faster), and a 3-stage ring of 32 KiB stages
+// (96 KiB) per CTA covers the loaded HBM latency and leaves room for two
+// CTAs per SM: thread-block clusters of up to 13 CTAs then fit once per
+// group for 16 groups, and the next launch's CTAs can be resident while this
+// one drains. Eight elements per lane (one 16-byte vector of a row) give each
+// warp more independent rows per tile than sixteen, and fewer registers for
+// the G query slices. With four or more the scores run on the tensor cores
+// and the CTA takes an SM to itself with a 5-stage ring (4 and 6 stages
+// measured slower on long single-sequence prefixes and the layers call).
 template <int D, int G>
 struct DecodeConfig {
   static constexpr int kWarps = 8;
   static constexpr int kPerLane = 8;
-  static constexpr int kStages = G >= 4 ? 4 : 3;
+  static constexpr int kStages = G >= 4 ? 5 : 3;
+  // Four or more query heads per KV head: the scores on the tensor cores
+  // (the CUDA-core score loop is instruction-bound there: about 560
+  // warp-instructions per consumer warp per 64-row tile, 48 GB/s per CTA;
+  // with tensor-core scores one CTA streams 64 GB/s, and a 5-stage ring
+  // keeps more bytes in flight behind the longer per-tile path).
+  static constexpr bool kTensorScores = G >= 4;
+};
+
+// Flavours of an instance with four or more query heads per KV head. The
+// default runs the scores on the tensor cores with one CTA per SM and a
+// 5-stage ring. kFlavorPair is the same with a 3-stage ring and a register
+// bound of two CTAs per SM (four heads per KV head only): a launch whose
+// groups already fill the GPU one CTA per group (the layers call) then runs
+// in one wave instead of two. kFlavorCudaCores keeps the scores on the CUDA
+// cores (4-stage ring): it reaches the first tile's output sooner, which
+// wins when each CTA streams only a few tiles. Instances with fewer heads per
+// KV head ignore the flavour (the same kernel). (kFlavor*: common.cuh.)
+template <int D, int G, int F>
+struct InstanceConfig {
+  static constexpr bool kTensorScores = DecodeConfig<D, G>::kTensorScores && F != kFlavorCudaCores;
+  static constexpr bool kTwoPerSm = F == kFlavorPair && kTensorScores && G <= 4;
+  static constexpr int kStages = kTwoPerSm ? 3 : kTensorScores ? DecodeConfig<D, G>::kStages : G >= 4 ? 4 : 3;
+  static constexpr int kMinBlocks = kTwoPerSm ? 2 : 1;
+  // The flavour this instance actually is (the kernel shared by flavours that coincide).
+  static constexpr int kFlavor = kTwoPerSm ? kFlavorPair : (G >= 4 && !kTensorScores) ? kFlavorCudaCores : kFlavorWide;
 };
 
 // Merge the per-warp (m, l, acc) states kept in shared memory for head g,
@@ -440,9 +498,10 @@ __device__ __forceinline__ void merge_partials_smem(const DecodeParams& p, int64
   }
 }
 
-template <typename T, int D, int G, int CW, int DPL, int NS, bool RP>
-__global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const DecodeParams p) {
-  using Shape = DecodeShape<D, G, CW, DPL, NS>;
+template <typename T, int D, int G, int CW, int DPL, int NS, bool RP, bool TC, int MB>
+__global__ void __launch_bounds__(DecodeShape<D, G, CW, DPL, NS, TC>::kThreads, MB)
+    decode_split_kernel(const __grid_constant__ DecodeParams p) {
+  using Shape = DecodeShape<D, G, CW, DPL, NS, TC>;
   constexpr int kStages = NS;
   using S = Storage<T>;
   constexpr int LPR = Shape::kLanesPerRow;
@@ -450,14 +509,28 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
   constexpr int CT = Shape::kConsumerThreads;
   constexpr int E = G * D;  // outputs of a group
 
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem_base[];
+  // With tensor-core scores the ring starts on a 1024-byte boundary (the
+  // atoms of the 128-byte swizzle the K tiles arrive in).
+  uint8_t* smem = TC ? smem_base + ((1024u - (smem_addr(smem_base) & 1023u)) & 1023u) : smem_base;
   float* red = reinterpret_cast<float*>(smem);  // per-warp states, once the ring is idle
   float* recv = reinterpret_cast<float*>(smem + Shape::kRingBytes);  // receive area of the cluster merge
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Shape::kBarOffset);
   uint64_t* empty = full + kStages;
   uint64_t* merge_bar = empty + kStages;  // the partials' bulk copies of the workspace merge
-  int* abort_flag = reinterpret_cast<int*>(merge_bar + 1);
+  uint64_t* sready = merge_bar + 1;       // tensor-core scores of a group's tile are in tensor memory [2]
+  uint64_t* sfree = sready + 2;           // a group has read them [2]
+  int* abort_flag = reinterpret_cast<int*>(merge_bar + 1 + (TC ? 4 : 0));
   int* last_flag = abort_flag + 1;
+  // Tensor-core scores (unused otherwise).
+  uint8_t* q_op = smem + Shape::kQOffset;                                  // the B operand
+  float* pw = reinterpret_cast<float*>(smem + Shape::kPOffset);            // [2][kTileRows][G] weights
+  float* gmax = reinterpret_cast<float*>(smem + Shape::kAuxOffset);        // [2][4][G]
+  float* lsum = gmax + 8 * G;                                              // [2][4][G]
+  float* mgrp = lsum + 8 * G;                                              // [2][G]
+  float* snew = mgrp + 2 * G;                                              // [G]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(snew + G);
+  constexpr uint32_t kTmemCols = 32;  // two 16-column score buffers
 
   const int s = blockIdx.x;
   const int g_kv = blockIdx.y;
@@ -488,6 +561,38 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
     const int cached = new_last ? rows - 1 : rows;
     uint8_t* kdst = smem + stage * Shape::kStageBytes;
     uint8_t* vdst = kdst + kTileBytes;
+    if constexpr (TC) {
+      // K arrives by tensor copies in the swizzled operand layout, whole
+      // tiles in one box per 64-column half, a partial tile in 8-row boxes
+      // (rows past the chunk are read but never weighted; the new row's
+      // score is computed apart, so the cache row L - 1 may hold anything).
+      // V arrives as in the other instances.
+      if (part != kSlotNew) {
+        // With rotary embedding the producer warp has already stored the new
+        // V row into this stage (rope_row): only the cached V rows arrive by TMA.
+        const int krows = rows == Shape::kTileRows ? rows : (rows + 7) / 8 * 8;
+        const int vrows = new_last && rope ? cached : rows;
+        mbar_arrive_expect_tx(&full[stage], (uint32_t)(krows + vrows) * Shape::kRowBytes);
+        const int z = b * p.n_kv_head + g_kv;
+        if (rows == Shape::kTileRows) {
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h)
+            tensor_load_3d(kdst + h * Shape::kTileRows * 128, &p.k_tiles, h * 64, tr0, z, &full[stage], policy);
+        } else {
+          for (int j = 0; j < krows / 8; ++j)
+#pragma unroll
+            for (int h = 0; h < D / 64; ++h)
+              tensor_load_3d(kdst + h * Shape::kTileRows * 128 + j * 1024, &p.k_rows8, h * 64, tr0 + 8 * j, z,
+                             &full[stage], policy);
+        }
+        if (cached > 0)
+          bulk_load(vdst, p.v_cache + (kv_row0 + tr0) * Shape::kRowBytes, cached * Shape::kRowBytes, &full[stage],
+                    policy);
+      }
+      if (new_last && !rope && part != kSlotCached)
+        bulk_load(vdst + cached * Shape::kRowBytes, p.v_new + new_row * 2, Shape::kRowBytes, &full[stage], policy);
+      return;
+    }
     if (part != kSlotNew) {
       // With rotary embedding the producer warp has already stored the new row
       // into this stage (rope_row): only the cached rows arrive by TMA.
@@ -511,8 +616,10 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
   // stores it, with the V row, as row `at` of the (free) stage of ring slot
   // u, before lane 0 issues that slot: the __syncwarp and lane 0's mbarrier
   // arrive (release) order these stores before the consumers' wait. With
-  // `to_cache` it also writes the rows into the cache at `pos`.
-  auto rope_row = [&](int pos, int u, int at, bool to_cache) {
+  // tensor-core scores only the V row goes into the stage (the new key's
+  // scores are computed apart). With `to_cache` it also writes the rows into
+  // the cache at `pos`; without `to_stage` it writes only the cache.
+  auto rope_row = [&](int pos, int u, int at, bool to_cache, bool to_stage = true) {
     uint4 kx = make_uint4(0u, 0u, 0u, 0u), vx = kx;
     float cs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, sn[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (lane < D / 8) {
@@ -525,8 +632,10 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
     if (lane < D / 8) {
       const uint4 kr = rope_vec8<T>(kx, ky, cs, sn, lane < D / 16);
       uint8_t* kdst = smem + (u % kStages) * Shape::kStageBytes + at * Shape::kRowBytes + lane * 16;
-      *reinterpret_cast<uint4*>(kdst) = kr;
-      *reinterpret_cast<uint4*>(kdst + kTileBytes) = vx;
+      if (to_stage) {
+        if (!TC) *reinterpret_cast<uint4*>(kdst) = kr;
+        *reinterpret_cast<uint4*>(kdst + kTileBytes) = vx;
+      }
       if (to_cache) {
         const int64_t dst = (kv_row0 + pos) * Shape::kRowBytes + lane * 16;
         *reinterpret_cast<uint4*>(p.k_cache_w + dst) = kr;
@@ -562,9 +671,15 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
     policy = evict_first_policy();
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], CW);
+      mbar_init(&empty[i], Shape::kEmptyArrivals);
     }
     mbar_init(merge_bar, 1);
+    if constexpr (TC) {
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&sready[i], 1);
+        mbar_init(&sfree[i], 1);
+      }
+    }
     *abort_flag = 0;
     fence_mbar_init();
     const int ch = chh;
@@ -600,7 +715,24 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
       }
     }
   }
+  if constexpr (TC) {
+    if (warp == CW + 1) {
+      tmem_alloc(tmem_slot, kTmemCols);
+      tc_fence_before();
+    }
+  }
   __syncthreads();
+  uint32_t tmem = 0;
+  if constexpr (TC) {
+    tc_fence_after();
+    tmem = *tmem_slot;
+  }
+  // The warp that allocated the tensor memory frees it before the CTA leaves.
+  auto free_tmem = [&]() {
+    if constexpr (TC) {
+      if (warp == CW + 1) tmem_free(tmem, kTmemCols);
+    }
+  };
   pdl_wait();
   // The next grid may be scheduled from here on: once it runs, every grid
   // before this one has completed.
@@ -638,7 +770,12 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
   const int lrow = lane / LPR;
   const int swap = Shape::kSwap ? (lrow & 1) : 0;
   uint4 qraw[G][NV];
-  if (warp < CW) {  // q loads overlap the length load below
+  uint4 q_chunk = make_uint4(0u, 0u, 0u, 0u);  // tensor-core scores: this thread's 16 bytes of the q operand
+  constexpr int kQChunks = D / 8;               // 16-byte chunks of a q row
+  if constexpr (TC) {
+    if (warp < CW && (int)threadIdx.x < 16 * kQChunks && (int)threadIdx.x / kQChunks < G)
+      q_chunk = ld_global_nc_v4(p.q + ((head0 + threadIdx.x / kQChunks) * D + (threadIdx.x % kQChunks) * 8) * 2);
+  } else if (warp < CW) {  // q loads overlap the length load below
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
@@ -666,6 +803,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
       if (threadIdx.x == 0 && p.err_flag) atomicOr(p.err_flag, err_bits);
     }
     drain_early();
+    free_tmem();
     return;
   }
   const int chunk = split_chunk(L, p.splits, Shape::kTileRows);
@@ -673,6 +811,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
   const int nclusters = (nsplit + CS - 1) / CS;  // clusters with at least one active split
   if (cid >= nclusters) {  // the whole cluster is idle
     drain_early();
+    free_tmem();
     return;
   }
   // Splits past nsplit in an active cluster read nothing and contribute an
@@ -690,9 +829,14 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
       load_f32x8(p.rope_cos, qpos, D, c * 8, qcos);
       load_f32x8(p.rope_sin, qpos, D, c * 8, qsin);
     }
+    if constexpr (TC) {
+      // This thread's chunk of the q operand: chunk c of its row (c = lane % LPR).
+      q_chunk = rope_vec8<T>(q_chunk, shfl_xor_v4(q_chunk, LPR / 2), qcos, qsin, c < LPR / 2);
+    } else {
 #pragma unroll
-    for (int g = 0; g < G; ++g) qraw[g][0] = rope_vec8<T>(qraw[g][0], shfl_xor_v4(qraw[g][0], LPR / 2), qcos, qsin,
-                                                          c < LPR / 2);
+      for (int g = 0; g < G; ++g)
+        qraw[g][0] = rope_vec8<T>(qraw[g][0], shfl_xor_v4(qraw[g][0], LPR / 2), qcos, qsin, c < LPR / 2);
+    }
   }
 
   // Cluster merge geometry: rank k of the cluster merges outputs
@@ -719,6 +863,85 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
     }
   };
 
+  if constexpr (TC) {
+    // The q operand: row h holds head h of the group (rows G..15 zero), in
+    // the 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r & 7)).
+    if (warp < CW) {
+      if ((int)threadIdx.x < 16 * kQChunks) {
+        const int row = threadIdx.x / kQChunks, ch = threadIdx.x % kQChunks;
+        *reinterpret_cast<uint4*>(q_op + (ch / 8) * 2048 + row * 128 + (((ch % 8) ^ (row & 7)) * 16)) = q_chunk;
+      }
+      if (warp == 0 && fused && r0 < r1 && r1 == L) {
+        // The new row is attended from k_new (the cache row L - 1 is being
+        // written by this launch): its scores on the CUDA cores, one 16-byte
+        // vector of k_new and q per lane (lane = chunk; with rotary
+        // embedding both rotated as above, lane c pairing with c ^ LPR / 2).
+        const bool in_row = lane < kQChunks;
+        const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+        uint4 kn = in_row ? ld_global_nc_v4(p.k_new + (new_row + lane * 8) * 2) : zero;
+        if (rope) kn = rope_vec8<T>(kn, shfl_xor_v4(kn, LPR / 2), qcos, qsin, c < LPR / 2);
+        float part[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          uint4 qv = in_row ? ld_global_nc_v4(p.q + ((head0 + g) * D + lane * 8) * 2) : zero;
+          if (rope) qv = rope_vec8<T>(qv, shfl_xor_v4(qv, LPR / 2), qcos, qsin, c < LPR / 2);
+          float a0 = 0.f, a1 = 0.f;
+          S::dot2(qv.x, kn.x, a0, a1);
+          S::dot2(qv.y, kn.y, a0, a1);
+          S::dot2(qv.z, kn.z, a0, a1);
+          S::dot2(qv.w, kn.w, a0, a1);
+          part[g] = in_row ? a0 + a1 : 0.f;
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) part[g] += __shfl_xor_sync(0xffffffffu, part[g], off);
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int g = 0; g < G; ++g) snew[g] = part[g] * p.qscale;
+        }
+      }
+      fence_proxy_async_shared();
+    }
+    if (warp != CW) named_barrier_sync<4, CT + 32>();  // consumers and the MMA warp: q operand staged
+  }
+
+  // Publication of this CTA's folded outputs (va, vm, vl per output
+  // threadIdx.x + k * CT): pushed to the cluster ranks, or emitted at once by
+  // a lone CTA. A CTA whose pipeline timed out publishes NaN, which poisons
+  // every output of its group.
+  auto publish = [&](const float (&va)[Shape::kPerThread], const float (&vm)[Shape::kPerThread],
+                     const float (&vl)[Shape::kPerThread], bool failed) {
+    const float nan = __int_as_float(0x7fc00000);
+    if (CS > 1) {
+      // Cluster plans: each folded value goes straight to the rank that
+      // merges it (distributed shared-memory stores), (m, l) of each head to
+      // every rank: the thread folding column r of the head sends them to
+      // rank r (every thread of a head holds that head's m and l).
+#pragma unroll
+      for (int k = 0; k < Shape::kPerThread; ++k) {
+        const int i = threadIdx.x + k * CT;
+        if (i < E) {
+          const int kk = i / per;
+          st_cluster_f32(acc_in + rank * per + (i - kk * per), kk, failed ? nan : va[k]);
+          const int g = i / D, r = i - g * D;
+          if (r < CS) {
+            st_cluster_f32(ml_in + rank * 2 * G + g, r, failed ? nan : vm[k]);
+            st_cluster_f32(ml_in + rank * 2 * G + G + g, r, vl[k]);
+          }
+        }
+      }
+    } else {
+      // A lone CTA: each folded output goes out (or into the workspace) at once.
+#pragma unroll
+      for (int k = 0; k < Shape::kPerThread; ++k) {
+        const int i = threadIdx.x + k * CT;
+        if (i < E) emit(i, failed ? nan : vm[k], vl[k], failed ? nan : va[k]);
+      }
+    }
+  };
+
   if (warp == CW) {
     // ---------------- producer warp ----------------
     if (fused && !rope && s == 0 && lane < D / 8) {
@@ -733,11 +956,15 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
       // Discarded early tiles: wait for them to land, then free their stages.
       for (int t = 0; t < spec; ++t) {
         if (!mbar_wait(&full[t], 0)) atomicOr(abort_flag, 1);
-        for (int w = 0; w < CW; ++w) mbar_arrive(&empty[t]);
+        for (int w = 0; w < Shape::kEmptyArrivals; ++w) mbar_arrive(&empty[t]);
       }
     }
     __syncwarp();
-    if (keep && spec_new >= 0 && lane < D / 8) {
+    if (TC && keep && spec_new >= 0) {
+      // The kept early slot spec_new holds the new V row but not the key
+      // row: both go into the cache from k_new / v_new again (rotated).
+      rope_row(L - 1, spec_new, 0, true, false);
+    } else if (keep && spec_new >= 0 && lane < D / 8) {
       // The kept early slot spec_new holds the rotated row of position L - 1
       // (its stage is not reused before the loop below): it goes into the
       // cache now. No CTA of this launch reads that row back from the cache.
@@ -790,6 +1017,248 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
       for (int u = max(0, next - kStages); u < next; ++u) mbar_wait(&full[u % kStages], (u / kStages) & 1);
     }
     __syncwarp();
+  } else if (warp == CW + 1) {
+    if constexpr (TC) {
+      // ---------------- MMA warp (tensor-core scores) ----------------
+      // Lane 0 issues the scores of tile t into buffer t & 1 once the tile
+      // has landed and the group that read the buffer's previous tile has
+      // released it: S^T = K q^T over D / 16 steps of 16 columns, then one
+      // commit that arrives on sready[t & 1] when the products are in
+      // tensor memory.
+      constexpr uint32_t idesc = mma_idesc_m128_n16(S::kBf16);
+      int issued = 0;
+      if (lane == 0) {
+        bool ok = true;
+        for (int t = 0; t < slot0 && ok; ++t) ok = mbar_wait(&full[t], 0);  // discarded early tiles
+        for (int t = 0; t < ntiles && ok; ++t) {
+          const int u = t + slot0;
+          const int stage = u % kStages;
+          ok = mbar_wait(&full[stage], (u / kStages) & 1);
+          if (ok && t >= 2) ok = mbar_wait(&sfree[t & 1], ((t - 2) >> 1) & 1);
+          if (!ok || *reinterpret_cast<volatile int*>(abort_flag)) break;
+          tc_fence_after();
+          const uint8_t* kd = smem + stage * Shape::kStageBytes;
+          const uint32_t dcol = tmem + (uint32_t)(t & 1) * 16u;
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const int h = k / 4, kk = k % 4;
+            mma_f16_ss(dcol, sw128_desc(kd + h * Shape::kTileRows * 128 + kk * 32),
+                       sw128_desc(q_op + h * 2048 + kk * 32), idesc, k > 0);
+          }
+          mma_commit(&sready[t & 1]);
+          issued = t + 1;
+        }
+        if (!ok) atomicOr(abort_flag, 1);
+      }
+      __syncwarp();
+      named_barrier_sync<4, CT + 32>();  // every consumer is done with the tensor memory
+      if (lane == 0) {
+        // Products still in flight after an abort land before the memory is freed.
+        for (int t = max(0, issued - 2); t < issued; ++t) mbar_wait(&sready[t & 1], (t >> 1) & 1);
+      }
+      __syncwarp();
+      tc_fence_after();
+      tmem_free(tmem, kTmemCols);
+    }
+  } else if constexpr (TC) {
+    // ---------------- consumer warps (tensor-core scores) ----------------
+    // Two groups of four warps take the tiles in turn (group t & 1 takes
+    // tile t), each with its own online-softmax state. In a tile, the
+    // group's first kTileRows threads each own one row (TMEM lane = row):
+    // they read its G scores from tensor memory, scale and mask them, and
+    // turn them into weights against the group's running max (raised, and
+    // the group's state rescaled, only when a score passes it by more than
+    // 2^kLazyRescale, decided by one barrier-reduction). The weights go
+    // through shared memory; then every thread of the group adds its rows'
+    // weighted V to its slice of the accumulators (D/8 threads per row, 16
+    // bytes of V each, packed fp32x2 FMAs), and the group releases the stage.
+    constexpr int TR = Shape::kTileRows;
+    constexpr int SW = TR / 32;                     // scoring warps of a group
+    constexpr int TPR = Shape::kVThreadsPerRow;
+    constexpr int RPT = Shape::kRowsPerThread;
+    constexpr int RG = Shape::kRowGroups;
+    const int grp = warp >> 2, gw = warp & 3, gt = (int)threadIdx.x & 127;
+    const bool scorer = gw < SW;
+    const int sw = gw;
+    const int vc = gt % TPR, rg = gt / TPR;
+    const uint32_t tcol = tmem + (uint32_t)grp * 16u + ((uint32_t)(gw * 32) << 16);
+    float* pg = pw + grp * TR * G;                  // this group's weights [TR][G]
+    // The group's barriers (IDs 2 and 3, 128 threads each).
+    auto group_sync = [&]() {
+      if (grp == 0) named_barrier_sync<2, 128>();
+      else named_barrier_sync<3, 128>();
+    };
+    auto group_or = [&](bool v) { return grp == 0 ? named_barrier_or<2, 128>(v) : named_barrier_or<3, 128>(v); };
+    float m[G], l_own[G];
+    float2 acc[G][4];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      m[g] = -INFINITY;
+      l_own[g] = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[g][e] = make_float2(0.f, 0.f);
+    }
+    // The tile whose last row is the new row (scores computed apart).
+    const int new_tile = (fused && r0 < r1 && r1 == L) ? ntiles - 1 : -1;
+    // Discarded early tiles: their copies must have landed (phase 0 of their
+    // stages) before a later phase of the same stages is waited for.
+    bool ok_pre = true;
+    for (int t = 0; t < slot0; ++t) ok_pre = mbar_wait(&full[t], 0) && ok_pre;
+    bool aborted = false;
+    for (int t = grp; t < ntiles; t += 2) {
+      const int u = t + slot0;
+      const int stage = u % kStages;
+      bool ok = ok_pre && mbar_wait(&full[stage], (u / kStages) & 1);
+      ok = ok && mbar_wait(&sready[grp], (t >> 1) & 1);
+      ok_pre = true;
+      if (group_or(!ok)) {
+        aborted = true;
+        break;
+      }
+      const int rows = min(TR, r1 - (r0 + t * TR));
+      float sc[G];
+      bool over = false;
+      if (scorer) {
+        tc_fence_after();
+        uint32_t raw[G];
+        tmem_load<G>(tcol, raw);
+        tc_fence_before();
+        const bool valid = gt < rows;
+#pragma unroll
+        for (int g = 0; g < G; ++g) sc[g] = valid ? __uint_as_float(raw[g]) * p.qscale : -INFINITY;
+        if (t == new_tile && gt == rows - 1) {
+#pragma unroll
+          for (int g = 0; g < G; ++g) sc[g] = snew[g];
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) over = over || sc[g] > m[g] + kLazyRescale;
+      }
+      const bool raise = group_or(over);
+      if (gt == 0) mbar_arrive(&sfree[grp]);  // the MMA warp may overwrite this buffer
+      if (raise) {
+        if (scorer) {
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            float x = sc[g];
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+            if (lane == 0) gmax[(grp * 4 + sw) * G + g] = x;
+          }
+        }
+        group_sync();
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float tm = gmax[(grp * 4) * G + g];
+#pragma unroll
+          for (int w = 1; w < SW; ++w) tm = fmaxf(tm, gmax[(grp * 4 + w) * G + g]);
+          const float mnew = fmaxf(m[g], tm);
+          const float alpha = (m[g] == -INFINITY) ? 0.f : fast_exp2(m[g] - mnew);
+          const float2 alpha2 = make_float2(alpha, alpha);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[g][e] = __fmul2_rn(acc[g][e], alpha2);
+          l_own[g] *= alpha;
+          m[g] = mnew;
+        }
+      }
+      if (scorer) {
+        float w[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          w[g] = (m[g] == -INFINITY) ? 0.f : fast_exp2(sc[g] - m[g]);
+          l_own[g] += w[g];
+        }
+#pragma unroll
+        for (int g = 0; g < G; g += 4)
+          *reinterpret_cast<float4*>(pg + gt * G + g) = make_float4(w[g], w[g + 1], w[g + 2], w[g + 3]);
+      }
+      group_sync();
+      // This thread's rows: [rg * RPT, (rg + 1) * RPT) of the tile.
+      const uint8_t* vt = smem + stage * Shape::kStageBytes + kTileBytes + vc * 16;
+      auto add_row = [&](int r) {
+        const uint4 vv = *reinterpret_cast<const uint4*>(vt + r * Shape::kRowBytes);
+        float2 vf[4];
+        S::unpack2(vv, vf);
+        float wr[G];
+#pragma unroll
+        for (int g = 0; g < G; g += 4) {
+          const float4 w4 = *reinterpret_cast<const float4*>(pg + r * G + g);
+          wr[g] = w4.x;
+          wr[g + 1] = w4.y;
+          wr[g + 2] = w4.z;
+          wr[g + 3] = w4.w;
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float2 w2 = make_float2(wr[g], wr[g]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[g][e] = __ffma2_rn(w2, vf[e], acc[g][e]);
+        }
+      };
+      if (rows == TR) {
+#pragma unroll
+        for (int j = 0; j < RPT; ++j) add_row(rg * RPT + j);
+      } else {
+        for (int j = 0; j < RPT && rg * RPT + j < rows; ++j) add_row(rg * RPT + j);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+    }
+    if (aborted) atomicOr(abort_flag, 1);
+    tc_fence_before();
+    named_barrier_sync<4, CT + 32>();  // the MMA warp may free the tensor memory
+
+    // Fold: the weight sums of each group's scoring threads, each group's
+    // running max, and the row groups' accumulators (over the idle ring).
+    if (scorer) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float x = l_own[g];
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+        if (lane == 0) lsum[(grp * 4 + sw) * G + g] = x;
+      }
+    }
+    if (gt == 0) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) mgrp[grp * G + g] = m[g];
+    }
+    named_barrier_sync<1, CT>();  // every consumer is done with the ring
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float* dst = red + ((grp * RG + rg) * G + g) * D + vc * 8;
+      *reinterpret_cast<float4*>(dst) = make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
+      *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[g][2].x, acc[g][2].y, acc[g][3].x, acc[g][3].y);
+    }
+    named_barrier_sync<1, CT>();
+    const bool failed = *reinterpret_cast<volatile int*>(abort_flag) != 0;
+    if (failed && threadIdx.x == 0 && p.err_flag) atomicOr(p.err_flag, kErrTimeout);
+    float va[Shape::kPerThread], vm[Shape::kPerThread], vl[Shape::kPerThread];
+#pragma unroll
+    for (int k = 0; k < Shape::kPerThread; ++k) {
+      const int i = threadIdx.x + k * CT;
+      if (i < E) {
+        const int g = i / D, d = i % D;
+        float mg[2], lg[2], ag[2];
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+          mg[q2] = mgrp[q2 * G + g];
+          float ls = 0.f, as = 0.f;
+#pragma unroll
+          for (int w = 0; w < SW; ++w) ls += lsum[(q2 * 4 + w) * G + g];
+#pragma unroll
+          for (int j = 0; j < RG; ++j) as += red[((q2 * RG + j) * G + g) * D + d];
+          lg[q2] = ls;
+          ag[q2] = as;
+        }
+        const float mm = fmaxf(mg[0], mg[1]);
+        const float f0 = (mg[0] == -INFINITY) ? 0.f : fast_exp2(mg[0] - mm);
+        const float f1 = (mg[1] == -INFINITY) ? 0.f : fast_exp2(mg[1] - mm);
+        vm[k] = mm;
+        vl[k] = lg[0] * f0 + lg[1] * f1;
+        va[k] = ag[0] * f0 + ag[1] * f1;
+      }
+    }
+    publish(va, vm, vl, failed);
   } else {
     // ---------------- consumer warps ----------------
     float m[G], l_own = 0.f;  // running max of every head; weight sum of this lane's head
@@ -905,33 +1374,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) decode_split_kernel(const De
       const int i = threadIdx.x + k * CT;
       if (i < E) merge_warps<D, G, CW>(red, i / D, i % D, &vm[k], &vl[k], &va[k]);
     }
-    const float nan = __int_as_float(0x7fc00000);
-    if (CS > 1) {
-      // Cluster plans: each folded value goes straight to the rank that
-      // merges it (distributed shared-memory stores), (m, l) of each head to
-      // every rank: the thread folding column r of the head sends them to
-      // rank r (every thread of a head holds that head's m and l).
-#pragma unroll
-      for (int k = 0; k < Shape::kPerThread; ++k) {
-        const int i = threadIdx.x + k * CT;
-        if (i < E) {
-          const int kk = i / per;
-          st_cluster_f32(acc_in + rank * per + (i - kk * per), kk, failed ? nan : va[k]);
-          const int g = i / D, r = i - g * D;
-          if (r < CS) {
-            st_cluster_f32(ml_in + rank * 2 * G + g, r, failed ? nan : vm[k]);
-            st_cluster_f32(ml_in + rank * 2 * G + G + g, r, vl[k]);
-          }
-        }
-      }
-    } else {
-      // A lone CTA: each folded output goes out (or into the workspace) at once.
-#pragma unroll
-      for (int k = 0; k < Shape::kPerThread; ++k) {
-        const int i = threadIdx.x + k * CT;
-        if (i < E) emit(i, failed ? nan : vm[k], vl[k], failed ? nan : va[k]);
-      }
-    }
+    publish(va, vm, vl, failed);
   }
 
   // ---------------- merge over the cluster ----------------

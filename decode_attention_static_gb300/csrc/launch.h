@@ -15,12 +15,14 @@ struct DecodeKernelInfo {
   int ctas_per_sm;
   int cluster_max;              // largest cluster size that can be resident
   int active_clusters[17];      // clusters of each size (1..16) resident at once
+  int tensor_scores;            // 1: the scores run on the tensor cores (K tiles by TMA tensor copies)
+  int flavor;                   // the flavour this kernel is (kFlavor* of decode_kernel.cuh)
 };
 
 bool decode_supported(int head_dim, int group);
 cudaError_t decode_kernel_info(int dtype, int head_dim, int group, int device, DecodeKernelInfo* info,
-                               bool rope = false);
-cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int group, cudaStream_t stream);
+                               bool rope = false, int flavor = 0);
+cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int group, int flavor, cudaStream_t stream);
 // Scratch bytes of one decode call with `splits` splits in clusters of
 // `cluster`: none when one cluster serves a group; otherwise a fixed region
 // of 32-bit arrival counters, then fp32 per-cluster partials
@@ -31,19 +33,20 @@ cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const
                           int32_t* err_flag, cudaStream_t stream);
 
 // Per-dtype halves of launch_decode / decode_kernel_info (one translation
-// unit each, compiled in parallel).
-cudaError_t launch_decode_f16(const DecodeParams& p, int head_dim, int group, cudaStream_t stream,
+// unit each, compiled in parallel); `flavor` selects the flavour where an
+// instance has several.
+cudaError_t launch_decode_f16(const DecodeParams& p, int head_dim, int group, int flavor, cudaStream_t stream,
                               const cudaLaunchAttribute* attr);
-cudaError_t launch_decode_bf16(const DecodeParams& p, int head_dim, int group, cudaStream_t stream,
+cudaError_t launch_decode_bf16(const DecodeParams& p, int head_dim, int group, int flavor, cudaStream_t stream,
                                const cudaLaunchAttribute* attr);
-cudaError_t decode_info_f16(int head_dim, int group, DecodeKernelInfo* info);
-cudaError_t decode_info_bf16(int head_dim, int group, DecodeKernelInfo* info);
+cudaError_t decode_info_f16(int head_dim, int group, int flavor, DecodeKernelInfo* info);
+cudaError_t decode_info_bf16(int head_dim, int group, int flavor, DecodeKernelInfo* info);
 // The same for the instances of the fused step with rotary embedding.
-cudaError_t launch_decode_f16_rope(const DecodeParams& p, int head_dim, int group, cudaStream_t stream,
+cudaError_t launch_decode_f16_rope(const DecodeParams& p, int head_dim, int group, int flavor, cudaStream_t stream,
                                    const cudaLaunchAttribute* attr);
-cudaError_t launch_decode_bf16_rope(const DecodeParams& p, int head_dim, int group, cudaStream_t stream,
+cudaError_t launch_decode_bf16_rope(const DecodeParams& p, int head_dim, int group, int flavor, cudaStream_t stream,
                                     const cudaLaunchAttribute* attr);
-cudaError_t decode_info_f16_rope(int head_dim, int group, DecodeKernelInfo* info);
-cudaError_t decode_info_bf16_rope(int head_dim, int group, DecodeKernelInfo* info);
+cudaError_t decode_info_f16_rope(int head_dim, int group, int flavor, DecodeKernelInfo* info);
+cudaError_t decode_info_bf16_rope(int head_dim, int group, int flavor, DecodeKernelInfo* info);
 
 }  // namespace da

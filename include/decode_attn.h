@@ -138,6 +138,26 @@ DA_API int decode_attn_workspace_init(void* workspace, size_t workspace_bytes, v
 DA_API int decode_attn_splits_for(int B, int n_head, int n_kv_head, int head_dim, int capacity,
                                   int max_kv_len_hint, int dtype, int* cluster_size);
 
+/* Kernels decode_attn_kernel_for reports. */
+#define DA_KERNEL_CUDA_CORES 0        /* scores on the CUDA cores (every group size) */
+#define DA_KERNEL_TENSOR_CORES 1      /* >= 4 query heads per KV head: scores on the tensor cores, one CTA per SM */
+#define DA_KERNEL_TENSOR_CORES_PAIRED 2 /* the same with two CTAs per SM (one CTA per group filling the GPU) */
+
+/*
+ * The decode kernel that decode_attn_fwd / decode_step_fwd / the layers call
+ * (rotary == 0) or decode_step_rope_fwd (rotary != 0) will launch for these
+ * arguments on the current device (for the layers call pass layers * B as
+ * B). With four or more query heads per KV head the scores of a K tile,
+ * q K^T, are a small dense product: the library runs it on the tensor cores
+ * when each CTA streams more than 8 tiles or when the groups fill the GPU one
+ * CTA each, and on the CUDA cores otherwise (shorter per-tile path). Every
+ * kernel computes the same softmax(q K^T * scale) V within the stated
+ * tolerance; results of different kernels may differ in the last bits.
+ * Returns a DA_KERNEL_* value or a negative da_status.
+ */
+DA_API int decode_attn_kernel_for(int B, int n_head, int n_kv_head, int head_dim, int capacity,
+                                  int max_kv_len_hint, int dtype, int rotary);
+
 /*
  * Profiling hook. When both are non-NULL, every later decode_attn_fwd /
  * decode_step_fwd call made by this host thread records event_before (a

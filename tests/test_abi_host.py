@@ -65,6 +65,12 @@ def test_plan_splits_properties(lib):
     # long prefix whose clusters would leave SMs idle (8 x 16 < 152): every
     # resident CTA streams rows, merged through the workspace
     assert da.plan_splits(1, 8, 128, 32768, sms, per) == (57, 1)
+    # one CTA per SM (four query heads per KV head): a split may stream up to
+    # 8 tiles and still be served by one cluster per group
+    assert da.plan_splits(1, 8, 128, 4096, sms, 1, cluster_max=12) == (12, 12)
+    assert da.plan_splits(1, 8, 128, 6144, sms, 1, cluster_max=12) == (12, 12)
+    assert da.plan_splits(1, 8, 128, 8192, sms, 1, cluster_max=12) == (19, 1)
+    assert da.plan_splits(1, 8, 128, 4096, sms, per, cluster_max=12) == (57, 1)
     # a batch: two waves' worth of splits (most sequences are shorter than the bound)
     assert da.plan_splits(8, 8, 128, 8192, sms, per) == (14, 1)
     # without clusters a short prefix is split flat too

@@ -142,12 +142,57 @@ def test_edge_lengths(ora, dtype, D, G):
     batch, with a NaN tail; both call styles."""
     tile = 8192 // (2 * D)
     Hkv = 2
-    lens = [1, 2, tile - 1, tile, tile + 1, 2 * tile + 3, 1000, 1531]
+    # 8-row steps (the tensor-core instances copy partial K tiles in 8-row
+    # boxes) and the 64- and 128-row tile edges
+    lens = [1, 2, 7, 8, 9, tile - 1, tile, tile + 1, 63, 64, 65, 127, 129, 2 * tile + 3, 1000, 1531]
     cap = max(lens) + 7
     pos = [L - 1 for L in lens]
     step = W.decode_step(len(lens), G * Hkv, Hkv, D, cap, dtype, pos, seed=D * 10 + G)
     for fused in FUSED:
         check_step(ora, step, fused, what=f"{dtype} D{D} G{G} fused={fused}")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("D", [64, 128])
+def test_many_groups_four_heads_per_kv_head(ora, dtype, D):
+    """More (sequence, KV head) groups than SMs with four query heads per KV
+    head: one CTA per group, run by the two-CTAs-per-SM kernel; ragged
+    lengths with 8-row and tile edges, NaN tail, both call styles."""
+    B, Hkv = 40, 4
+    rng = np.random.default_rng(D + (1 if dtype == "bf16" else 0))
+    lens = [1, 7, 8, 9, 63, 64, 65, 127, 128, 129, 700] + rng.integers(1, 701, B - 11).tolist()
+    step = W.decode_step(B, 4 * Hkv, Hkv, D, 707, dtype, [L - 1 for L in lens], seed=90 + D)
+    for fused in FUSED:
+        check_step(ora, step, fused, what=f"{dtype} D{D} B{B} fused={fused}")
+
+
+# (B, n_head, n_kv_head, head_dim, capacity, kernel): one case per kernel and
+# group size, lengths ragged up to the capacity, bound = capacity.
+KERNEL_CASES = [
+    (1, 32, 8, 128, 4096, "cuda_cores"),          # 6 tiles per CTA
+    (1, 32, 8, 128, 20000, "tensor_cores"),       # 17 tiles per CTA
+    (1, 32, 8, 64, 40000, "tensor_cores"),
+    (1, 16, 2, 128, 70000, "tensor_cores"),       # eight heads per KV head
+    (1, 16, 2, 64, 140000, "tensor_cores"),
+    (40, 16, 4, 128, 700, "tensor_cores_paired"),  # 160 groups, one CTA each
+    (40, 16, 4, 64, 700, "tensor_cores_paired"),
+    (24, 64, 8, 128, 700, "tensor_cores"),        # 192 groups of eight heads: no paired kernel
+]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("case", KERNEL_CASES, ids=[f"{c[5]}-G{c[1] // c[2]}-D{c[3]}-B{c[0]}" for c in KERNEL_CASES])
+def test_each_kernel(ora, dtype, case):
+    """Every decode kernel the library chooses between, against the oracle:
+    the case must select the kernel it is meant to cover."""
+    B, H, Hkv, D, cap, kernel = case
+    tdt = torch.float16 if dtype == "f16" else torch.bfloat16
+    assert da.kernel_for(B, H, Hkv, D, cap, cap, tdt) == kernel
+    rng = np.random.default_rng(cap + D + B)
+    lens = [cap] + rng.integers(1, cap + 1, B - 1).tolist()
+    step = W.decode_step(B, H, Hkv, D, cap, dtype, [L - 1 for L in lens], seed=cap % 1000 + D)
+    for fused in FUSED:
+        check_step(ora, step, fused, hint=cap, what=f"{kernel} {dtype} G{H // Hkv} D{D} fused={fused}")
 
 
 def test_capacity_one_and_full(ora):
