@@ -173,11 +173,11 @@ bool encode_k_maps(DecodeParams* p, const void* k_cache, int dtype, int64_t grou
 // the instances with four or more heads per KV head: its per-tile path is
 // shorter (no tensor-memory round trip), which wins until the tensor-core
 // flavour's higher streaming rate pays (measured, 32 / 8 heads, one
-// sequence: kv 256 / 1024 / 3072 / 6144 / 8192 at 1 / 2 / 4 / 8 / 7 tiles per
-// CTA take 4.22 / 5.27 / 7.02 / 9.74 / 11.1 us instead of 5.36 / 6.32 / 7.42
-// / 10.16 / 11.2; at kv 16384 and 32768, 14 and 27 tiles per CTA, the
-// tensor-core flavour takes 15.7 and 25.5 us instead of 16.5 and 26.2).
-constexpr int64_t kCudaCoreChunkTiles = 8;
+// sequence, µs per call CUDA-core / tensor-core: kv 1024 and 2048, 2 and 3
+// tiles per CTA, 5.30 / 6.14 and 6.30 / 6.43; kv 4096, 12288, 16384 and
+// 32768, 6, 11, 14 and 27 tiles, 8.22 / 7.90, 13.97 / 13.54, 16.55 / 15.86
+// and 26.45 / 25.25).
+constexpr int64_t kCudaCoreChunkTiles = 4;
 
 // Splits and cluster size for the current device: plan + occupancy of the
 // instance. *flavor (if given) gets the flavour of the instance the call

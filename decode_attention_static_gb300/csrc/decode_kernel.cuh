@@ -1026,6 +1026,11 @@ __global__ void __launch_bounds__(DecodeShape<D, G, CW, DPL, NS, TC>::kThreads, 
       // commit that arrives on sready[t & 1] when the products are in
       // tensor memory.
       constexpr uint32_t idesc = mma_idesc_m128_n16(S::kBf16);
+      // Descriptors of the ring's first byte and of the q operand; an
+      // operand at byte offset o from them is the descriptor + o / 16 (the
+      // start-address field; every address stays below 256 KiB).
+      const uint64_t a_base = sw128_desc(smem);
+      const uint64_t b_base = sw128_desc(q_op);
       int issued = 0;
       if (lane == 0) {
         bool ok = true;
@@ -1037,13 +1042,13 @@ __global__ void __launch_bounds__(DecodeShape<D, G, CW, DPL, NS, TC>::kThreads, 
           if (ok && t >= 2) ok = mbar_wait(&sfree[t & 1], ((t - 2) >> 1) & 1);
           if (!ok || *reinterpret_cast<volatile int*>(abort_flag)) break;
           tc_fence_after();
-          const uint8_t* kd = smem + stage * Shape::kStageBytes;
+          const uint64_t a_stage = a_base + (uint64_t)((stage * Shape::kStageBytes) >> 4);
           const uint32_t dcol = tmem + (uint32_t)(t & 1) * 16u;
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const int h = k / 4, kk = k % 4;
-            mma_f16_ss(dcol, sw128_desc(kd + h * Shape::kTileRows * 128 + kk * 32),
-                       sw128_desc(q_op + h * 2048 + kk * 32), idesc, k > 0);
+            mma_f16_ss(dcol, a_stage + (uint64_t)((h * Shape::kTileRows * 128 + kk * 32) >> 4),
+                       b_base + (uint64_t)((h * 2048 + kk * 32) >> 4), idesc, k > 0);
           }
           mma_commit(&sready[t & 1]);
           issued = t + 1;
@@ -1105,20 +1110,24 @@ __global__ void __launch_bounds__(DecodeShape<D, G, CW, DPL, NS, TC>::kThreads, 
     bool ok_pre = true;
     for (int t = 0; t < slot0; ++t) ok_pre = mbar_wait(&full[t], 0) && ok_pre;
     bool aborted = false;
+    volatile int* grp_abort = reinterpret_cast<volatile int*>(last_flag + 1 + grp);  // a wait of the group gave up
+    if (gt == 0) *grp_abort = 0;
+    group_sync();
     for (int t = grp; t < ntiles; t += 2) {
       const int u = t + slot0;
       const int stage = u % kStages;
       bool ok = ok_pre && mbar_wait(&full[stage], (u / kStages) & 1);
       ok = ok && mbar_wait(&sready[grp], (t >> 1) & 1);
       ok_pre = true;
-      if (group_or(!ok)) {
-        aborted = true;
-        break;
-      }
+      // A warp reads the scores only if all its lanes' waits succeeded (the
+      // load is warp-wide); the group learns of a failed wait after the
+      // barrier below, which also decides the raise.
+      const bool warp_ok = __all_sync(0xffffffffu, ok);
+      if (!warp_ok && lane == 0) *grp_abort = 1;
       const int rows = min(TR, r1 - (r0 + t * TR));
       float sc[G];
       bool over = false;
-      if (scorer) {
+      if (scorer && warp_ok) {
         tc_fence_after();
         uint32_t raw[G];
         tmem_load<G>(tcol, raw);
@@ -1134,6 +1143,10 @@ __global__ void __launch_bounds__(DecodeShape<D, G, CW, DPL, NS, TC>::kThreads, 
         for (int g = 0; g < G; ++g) over = over || sc[g] > m[g] + kLazyRescale;
       }
       const bool raise = group_or(over);
+      if (*grp_abort) {
+        aborted = true;
+        break;
+      }
       if (gt == 0) mbar_arrive(&sfree[grp]);  // the MMA warp may overwrite this buffer
       if (raise) {
         if (scorer) {

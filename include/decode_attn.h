@@ -149,7 +149,7 @@ DA_API int decode_attn_splits_for(int B, int n_head, int n_kv_head, int head_dim
  * arguments on the current device (for the layers call pass layers * B as
  * B). With four or more query heads per KV head the scores of a K tile,
  * q K^T, are a small dense product: the library runs it on the tensor cores
- * when each CTA streams more than 8 tiles or when the groups fill the GPU one
+ * when each CTA streams more than 4 tiles or when the groups fill the GPU one
  * CTA each, and on the CUDA cores otherwise (shorter per-tile path). Every
  * kernel computes the same softmax(q K^T * scale) V within the stated
  * tolerance; results of different kernels may differ in the last bits.

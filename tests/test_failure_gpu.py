@@ -32,12 +32,17 @@ def _run(step, hint, ws):
     return out, int(err.item())
 
 
-@pytest.mark.parametrize("case", ["flat", "cluster"])
+@pytest.mark.parametrize("case", ["flat", "cluster", "gqa_cluster"])
 def test_pipeline_timeout_is_reported_and_the_context_survives(ora, case):
     if case == "flat":
-        step, hint = W.long_context(seed=40), 32768        # flat split plan, merge through the workspace
-    else:
+        # flat split plan, merge through the workspace; tensor-core scores
+        step, hint = W.long_context(seed=40), 32768
+    elif case == "cluster":
         step, hint = W.mha_sweep(4096, seed=41), 4096      # one cluster per head, on-chip merge
+    else:
+        # four heads per KV head, one cluster per group, CUDA-core scores
+        step, hint = W.long_context(seed=42, kv_len=2048, capacity=2048), 2048
+        assert da.kernel_for(1, step.n_head, step.n_kv_head, step.head_dim, 2048, 2048, step.q.dtype) == "cuda_cores"
     G = step.n_head // step.n_kv_head
     ws = da.alloc_workspace(step.B, step.n_head, step.n_kv_head, step.head_dim, step.capacity)
     da.test_skip_slot(1)

@@ -169,7 +169,7 @@ def test_many_groups_four_heads_per_kv_head(ora, dtype, D):
 # (B, n_head, n_kv_head, head_dim, capacity, kernel): one case per kernel and
 # group size, lengths ragged up to the capacity, bound = capacity.
 KERNEL_CASES = [
-    (1, 32, 8, 128, 4096, "cuda_cores"),          # 6 tiles per CTA
+    (1, 32, 8, 128, 2048, "cuda_cores"),          # 3 tiles per CTA
     (1, 32, 8, 128, 20000, "tensor_cores"),       # 17 tiles per CTA
     (1, 32, 8, 64, 40000, "tensor_cores"),
     (1, 16, 2, 128, 70000, "tensor_cores"),       # eight heads per KV head
