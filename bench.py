@@ -715,7 +715,8 @@ def kv_curve(torch, da, device, l2_bytes: int) -> list:
         us = graph_us_per_call(torch, device, issue, layers, reps=max(3, 2000 // layers))
         b = attend_bytes(1, H, Hkv, D, [kv], 2) + append_bytes(1, Hkv, D, 2)
         s, cs = da.splits_for(1, H, Hkv, D, kv, kv, dt)
-        res.append({"kv_len": kv, "layers": layers, "splits": s, "cluster": cs, "us_per_layer_step": round(us, 3),
+        res.append({"kv_len": kv, "layers": layers, "splits": s, "cluster": cs,
+                    "kernel": da.kernel_for(1, H, Hkv, D, kv, kv, dt), "us_per_layer_step": round(us, 3),
                     "gbs": round(b / (us * 1e-6) / 1e9, 1)})
         del k, v
     return res
@@ -798,7 +799,9 @@ def other_configs(torch, da, device, l2_bytes: int) -> dict:
             da.decode_step_fwd(t.q, t.k_cache, t.v_cache, t.k_new, t.v_new, t.position_ids, workspace=ws,
                                max_kv_len_hint=t_hint)
 
-    res["tiny_gqa"] = {"us_per_layer_step": round(graph_us_per_call(torch, device, issue_tiny, 64, 50), 3)}
+    res["tiny_gqa"] = {"us_per_layer_step": round(graph_us_per_call(torch, device, issue_tiny, 64, 50), 3),
+                       "kernel": da.kernel_for(t.B, t.n_head, t.n_kv_head, t.head_dim, t.capacity, t_hint,
+                                               t.q.dtype)}
 
     # batched streaming: B=8, 16 / 8 heads, capacity 8192, ragged lengths; three
     # copies of the caches rotate so that consecutive calls read cold HBM
@@ -819,7 +822,9 @@ def other_configs(torch, da, device, l2_bytes: int) -> dict:
     b = attend_bytes(s0.B, s0.n_head, s0.n_kv_head, s0.head_dim, kvs, 2) + append_bytes(s0.B, s0.n_kv_head,
                                                                                         s0.head_dim, 2)
     res["batched_streaming"] = {"us_per_layer_step": round(us, 3), "gbs": round(b / (us * 1e-6) / 1e9, 1),
-                                "sum_kv_len": int(sum(kvs))}
+                                "sum_kv_len": int(sum(kvs)),
+                                "kernel": da.kernel_for(s0.B, s0.n_head, s0.n_kv_head, s0.head_dim, s0.capacity,
+                                                        hint, s0.q.dtype)}
     del kc, vc, s0
 
     # S2-Pro-shaped generation: every layer's step at three positions of the
@@ -853,7 +858,9 @@ def other_configs(torch, da, device, l2_bytes: int) -> dict:
         lw = graph_us_per_call(torch, device, issue_layers, 1, 200) / layers
         lc = graph_us_per_call(torch, device, issue_layers, 1, 20, flush=flush) / layers
         b = attend_bytes(1, H, Hkv, D, [kv], 2) + append_bytes(1, Hkv, D, 2)
-        gen_res.append({"kv_len": kv, "us_per_layer_step_as_run": round(warm, 3),
+        gen_res.append({"kv_len": kv, "kernel": da.kernel_for(1, H, Hkv, D, cap, kv, dt),
+                        "layers_call_kernel": da.kernel_for(layers, H, Hkv, D, cap, kv, dt),
+                        "us_per_layer_step_as_run": round(warm, 3),
                         "us_per_layer_step_l2_flushed": round(cold, 3),
                         "gbs_l2_flushed": round(b / (cold * 1e-6) / 1e9, 1),
                         "layers_call_us_per_layer_step_as_run": round(lw, 3),
