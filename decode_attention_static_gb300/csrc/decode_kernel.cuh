@@ -3,7 +3,9 @@
 // One CTA per (split s, KV head g, sequence b). It owns the rows
 // [s * chunk, min((s + 1) * chunk, L)) of its sequence's K and V, where L is
 // the active length and chunk an even share of L in whole tiles, so every
-// byte of the active prefix is read exactly once and nothing beyond it. The
+// byte of the active prefix is read exactly once (the tensor-core variant
+// below copies a partial last K tile in 8-row boxes: at most 7 rows past the
+// prefix, never weighted). The
 // CTA serves all G query heads of its KV head from that single read
 // (grouped-query attention without expansion: fish-speech issue #1310,
 // section 2; VoxCPM issue #395, section 4.1, enable_gqa).
@@ -21,6 +23,13 @@
 // implementation"). The fused step reads the attended row L - 1 from k_new
 // and v_new and writes it into the cache; with rotary embedding (RP) q and
 // that key row are rotated first (VoxCPM issue #395, section 4.1).
+//
+// Tensor-core scores (TC, four or more query heads per KV head): the scores
+// of a K tile are one tcgen05.mma chain (S^T = K q^T, fp32 in tensor memory)
+// issued by an extra warp, K arriving by TMA tensor copies in the swizzled
+// operand layout; two groups of four consumer warps take the tiles in turn,
+// read the scores from tensor memory and accumulate the weighted V on the
+// CUDA cores (see the TC consumer below).
 //
 // Merge of the splits. The splits of one (b, g) group are launched as
 // thread-block clusters of `cluster` CTAs. Each CTA folds its warps' states
