@@ -152,8 +152,11 @@ DA_API int decode_attn_splits_for(int B, int n_head, int n_kv_head, int head_dim
  * when each CTA streams more than 4 tiles or when the groups fill the GPU one
  * CTA each, and on the CUDA cores otherwise (shorter per-tile path). Every
  * kernel computes the same softmax(q K^T * scale) V within the stated
- * tolerance; results of different kernels may differ in the last bits.
- * Returns a DA_KERNEL_* value or a negative da_status.
+ * tolerance (the operation of decode_attn_fwd: Cuda-Compute-OSS issue #343,
+ * "Proposed implementation"); results of different kernels may differ in
+ * the last bits. Sizes are validated as in decode_attn_fwd (DA_ERR_SHAPE,
+ * DA_ERR_UNSUPPORTED, DA_ERR_DTYPE before any device query). Returns a
+ * DA_KERNEL_* value or a negative da_status.
  */
 DA_API int decode_attn_kernel_for(int B, int n_head, int n_kv_head, int head_dim, int capacity,
                                   int max_kv_len_hint, int dtype, int rotary);

@@ -173,6 +173,15 @@ def test_valid_call_without_gpu_reports_cuda_error(lib):
     assert lib.decode_attn_workspace_size(1, 32, 8, 128, 1024) == ctypes.c_size_t(-1).value
 
 
+def test_kernel_for_rejects_bad_sizes_without_a_device(lib):
+    # validated before any device query: group size, head_dim, dtype
+    assert lib.decode_attn_kernel_for(1, 30, 8, 128, 1024, 0, 1, 0) == -2   # n_head % n_kv_head
+    assert lib.decode_attn_kernel_for(1, 32, 8, 96, 1024, 0, 1, 0) == -3    # unsupported head_dim
+    assert lib.decode_attn_kernel_for(1, 48, 4, 128, 1024, 0, 1, 0) == -3   # unsupported group size 12
+    assert lib.decode_attn_kernel_for(1, 32, 8, 128, 1024, 0, 7, 0) == -7   # unknown dtype
+    assert lib.decode_attn_kernel_for(0, 32, 8, 128, 1024, 0, 1, 0) == 0    # empty batch: nothing launched
+
+
 def test_workspace_size_rejects_bad_sizes(lib):
     assert lib.decode_attn_workspace_size(1, 30, 8, 128, 1024) == ctypes.c_size_t(-1).value
     assert lib.decode_attn_workspace_size(1, 32, 8, 100, 1024) == ctypes.c_size_t(-1).value
