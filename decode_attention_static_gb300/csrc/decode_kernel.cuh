@@ -137,7 +137,7 @@ struct DecodeConfig {
   // Four or more query heads per KV head: the scores on the tensor cores
   // (the CUDA-core score loop is instruction-bound there: about 560
   // warp-instructions per consumer warp per 64-row tile, 48 GB/s per CTA;
-  // with tensor-core scores one CTA streams 64 GB/s, and a 5-stage ring
+  // with tensor-core scores one CTA streams 70 GB/s, and a 5-stage ring
   // keeps more bytes in flight behind the longer per-tile path).
   static constexpr bool kTensorScores = G >= 4;
 };
