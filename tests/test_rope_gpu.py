@@ -105,18 +105,19 @@ def test_position_zero_returns_v_new(dtype):
     assert torch.equal(out.view(torch.int16), want.contiguous().view(torch.int16))
 
 
-@pytest.mark.parametrize("shape", [(2, 1500, [1499, 700], "cuda_cores"), (1, 20000, [19999], "tensor_cores"),
-                                   (40, 700, None, "tensor_cores_paired")], ids=lambda s: s[3])
+@pytest.mark.parametrize("shape", [(2, 1500, [1499, 700], 128, "cuda_cores"), (1, 20000, [19999], 128, "tensor_cores"),
+                                   (1, 40000, [39998], 64, "tensor_cores"), (40, 700, None, 128, "tensor_cores_paired")],
+                         ids=lambda s: f"{s[4]}-D{s[3]}")
 def test_matches_unrotated_step_on_rotated_inputs(ora, shape):
     """The fused rotation is bit-identical to rotating q and k_new with the
     oracle and running the plain fused step: same cache, same output bits
     (32 / 8 heads, bf16; each of the kernels the library chooses between)."""
-    B, cap, pos, kernel = shape
+    B, cap, pos, D, kernel = shape
     if pos is None:
         pos = np.random.default_rng(5).integers(0, cap, B).tolist()
-    assert da.kernel_for(B, 32, 8, 128, cap, 0, torch.bfloat16, rotary=True) == kernel
-    assert da.kernel_for(B, 32, 8, 128, cap, 0, torch.bfloat16) == kernel
-    step = W.decode_step(B, 32, 8, 128, cap, "bf16", pos, seed=32)
+    assert da.kernel_for(B, 32, 8, D, cap, 0, torch.bfloat16, rotary=True) == kernel
+    assert da.kernel_for(B, 32, 8, D, cap, 0, torch.bfloat16) == kernel
+    step = W.decode_step(B, 32, 8, D, cap, "bf16", pos, seed=32)
     cos, sin = tables(step, "random")
     q_rot, k_rot, _, _, _ = oracle_rope_step(ora, step, cos, sin)
     d_rope, out_rope, err = gpu_rope_step(step, cos, sin)
